@@ -1,0 +1,357 @@
+"""Benchmark of the fused gradient all-reduce on one GB300 (or N replicas).
+
+Metric: all-reduce GB/s on the algorithmic minimum of HBM traffic, 2*P*N*e
+bytes per all-reduce (every rank element read once and written once), plus
+elements/s, per schedule; and the fraction of the measured HBM copy bandwidth.
+
+    python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--mode fused|stepwise|rankorder]
+                    [--kernel auto|ldg|bulk] [--impl ours|reference] [--no-e2e] [--no-cpu]
+
+A "step" is one ddl_allreduce of the whole gradient (every bucket).  The
+default workload is the 4x4 2D-torus all-reduce of a ResNet-50 gradient
+(P=16 ranks x 25,557,032 fp32, scale 1/16; 1.64 GB resident, well above the
+129 MB L2, so every step streams from HBM).  With --gpus N > 1 (torchrun) the
+path does not shard: each GPU runs an independent replica, and the reported
+value is the total over all replicas.  --impl reference times the oracle (the
+plain single-threaded CPU emulation) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "all-reduce GB/s and elems/s per schedule on 1 GB300; % of HBM roofline"
+DEFAULT_WORKLOAD = "torus4x4_resnet50"
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the fused kernel,
+# from one ncu capture, keyed by (workload, kernel variant, sha256[:16] of the
+# kernel source it was taken on).  A changed kernel reports null.
+NCU_TRAFFIC = {}
+
+KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def schedule_name(w) -> str:
+    if w.topo == "torus":
+        return f"torus {w.X}x{w.Y}"
+    if w.topo == "multiring":
+        return f"multi-ring k={w.k}"
+    return "ring"
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.6)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.3)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t0 - 1 <= r[0] <= self.t1 + 1] or rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            for n, v in zip(names, r[3]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        sm = [r[1] for r in inside]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def cpu_baseline(w, target_s: float = 6.0, max_elems: int = 2_000_000):
+    """The oracle as it stands (single thread) on a bounded sample of the
+    workload: same P, schedule, dtype and value distribution, the first
+    `max_elems` elements per rank as one bucket; repeated until `target_s`."""
+    import oracle
+    n = min(w.N, max_elems)
+    host = [synth.draw_rank(w.seed, r, n, w.dist, w.sigma, w.dtype) for r in range(w.P)]
+    layers = None
+    if w.layers is not None:
+        acc, layers = 0, []
+        for v in w.layers:
+            if acc >= n:
+                break
+            layers.append(min(v, n - acc))
+            acc += layers[-1]
+    cfg = oracle.Config(w.P, n, w.dtype, w.topo, k=w.k, X=w.X, Y=w.Y, bucket_bytes=w.bucket_bytes, layers=layers)
+    spent, reps = 0.0, 0
+    while spent < target_s or reps < 1:
+        bufs = [h.copy() for h in host]
+        t = time.perf_counter()
+        oracle.emulate(cfg, bufs, w.scale)
+        spent += time.perf_counter() - t
+        reps += 1
+    per = spent / reps
+    gbs = 2 * w.P * n * w.esize / per / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{w.P} ranks x {n} elements ({schedule_name(w)}, {w.dtype}), {reps} runs, "
+                      f"{per * 1e3:.1f} ms per run, single-threaded step emulation",
+            "elems_per_s": round(w.P * n / per, 1)}
+
+
+def smi_gpu_id(local: int) -> str:
+    """nvidia-smi --id for this process's GPU (index or UUID)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids):
+            return ids[local]
+    return str(local)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    # per-step sample sized so that K + W steps take about two minutes at the
+    # oracle's ~8 ns per rank-element (copies included)
+    budget_s = 120.0
+    n = int(budget_s / ((args.steps + args.warmup) * w.P * 8e-9))
+    n = max(4096, min(n, w.N, 2_000_000))
+    host = [synth.draw_rank(w.seed, r, n, w.dist, w.sigma, w.dtype) for r in range(w.P)]
+    cfg = oracle.Config(w.P, n, w.dtype, w.topo, k=w.k, X=w.X, Y=w.Y)
+    times = []
+    for i in range(args.warmup + args.steps):
+        bufs = [h.copy() for h in host]
+        t = time.perf_counter()
+        oracle.emulate(cfg, bufs, w.scale)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t)
+    per = sum(times) / len(times)
+    gbs = 2 * w.P * n * w.esize / per / 1e9
+    sample = (f"oracle on {w.P} ranks x {n} elements of {w.name} ({schedule_name(w)}, {w.dtype}) per step, "
+              f"single-threaded")
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic", "config": {"workload": w.name, "P": w.P, "N": w.N, "schedule": schedule_name(w),
+                                            "sample_elems_per_rank": n},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--mode", default="fused", choices=["fused", "stepwise", "rankorder"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "ldg", "bulk"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+
+    from gradient_all_reduce_ddl_gb300 import ddl
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    tdt = torch.float16 if w.dtype == "f16" else torch.float32
+    bufs = []
+    for r in range(w.P):
+        t = torch.empty(w.N, dtype=tdt, device=dev)
+        synth.fill_device(t.data_ptr(), w.N, w.seed, r, w.dist, w.sigma, w.dtype, stream=stream.cuda_stream)
+        bufs.append(t)
+    plan = ddl.Plan.for_workload(w, mode=args.mode, kernel=args.kernel)
+    nbytes = w.min_bytes
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        plan.allreduce(bufs, w.scale, stream)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(smi_gpu_id(local if ws > 1 else 0))
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches0 = plan.launches
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.mark("t0")
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        plan.allreduce(bufs, w.scale, stream)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks.mark("t1")
+    clk = clocks.stop()
+    launches = plan.launches - launches0
+    total_ms = start.elapsed_time(end)
+    per_call_ms = [a.elapsed_time(b) for a, b in ev]
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    gbs = nbytes * ws / (ms_per_step * 1e-3) / 1e9
+    elems = w.P * w.N * ws / (ms_per_step * 1e-3)
+
+    # roofline of the dominant kernel: one fused launch per bucket
+    nb = plan.num_buckets
+    launches_per_call = max(1, launches // args.steps)
+    avg_call_ms = statistics.mean(per_call_ms)
+    peak, peak_kind = measured_peak()
+    kernel_name = {"fused": "fold_ldg_kernel" if args.kernel != "bulk" else "fold_bulk_kernel",
+                   "rankorder": "fold_ldg_kernel (rank order)", "stepwise": "step_kernel"}[args.mode]
+    if args.mode == "stepwise":
+        achieved = None
+    else:
+        achieved = nbytes / (avg_call_ms * 1e-3) / 1e9  # bytes of all buckets / time of the call
+    traffic = NCU_TRAFFIC.get((w.name, args.kernel if args.kernel != "auto" else "ldg", kernel_hash()))
+    roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": None if achieved is None else round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": None if achieved is None else round(achieved / peak, 4),
+                "peak_kind": f"hbm_gbs of {peak_kind}", "traffic": traffic,
+                "algorithmic_bytes_per_launch": nbytes // max(1, nb), "launches_per_step": launches_per_call,
+                "avg_call_ms": round(avg_call_ms, 4)}
+
+    # end to end through the C ABI with page-locked host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = [torch.empty(w.N, dtype=tdt, pin_memory=True) for _ in range(w.P)]
+        for r in range(w.P):
+            host[r].copy_(bufs[r])
+        torch.cuda.synchronize(dev)
+        plan.allreduce_host(host, bufs, w.scale, stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.e2e_steps):
+            plan.allreduce_host(host, bufs, w.scale, stream)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = s0.elapsed_time(s1) / args.e2e_steps
+        te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        if ws > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e_ms = float(te.item())
+        e2e = {"value": round(nbytes * ws / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": w.P * w.N * w.esize, "d2h_bytes_per_step": w.P * w.N * w.esize,
+               "ms_per_step": round(e2e_ms, 3), "steps": args.e2e_steps,
+               "path": "ddl_allreduce_host: H2D copies + fused all-reduce + D2H copies on one stream"}
+        del host
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+                "config": {"workload": w.name, "P": w.P, "N": w.N, "schedule": schedule_name(w), "mode": args.mode,
+                           "kernel": args.kernel, "buckets": nb, "bytes_per_step": nbytes,
+                           "elems_per_s": round(elems, 1), "frac_of_hbm": round(gbs / ws / peak, 4),
+                           "l2": f"inputs {w.P * w.N * w.esize / 1e9:.2f} GB per replica, larger than the 129 MB L2",
+                           "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU, P logical ranks"},
+                "clocks": clk, "gpu_launches": launches, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
+                "kernel_src": kernel_hash()}
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

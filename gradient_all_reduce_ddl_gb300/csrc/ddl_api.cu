@@ -1,0 +1,428 @@
+// ddl_api.cu -- the C ABI declared in include/ddl.h.
+//
+// A plan holds the host tables (plan.cpp), their device copies, the side
+// stream and the per-bucket events.  Every entry point validates its
+// arguments before queueing anything, maps CUDA failures to DDL_ERR_CUDA, and
+// never throws across the ABI.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "ddl.h"
+#include "kernels.h"
+#include "plan.h"
+
+struct ddl_plan {
+  ddl::Spec spec;
+  ddl::Tables tab;
+  int kernel = DDL_KERNEL_AUTO;
+  // device side
+  int device = -1;
+  bool dev_current = false;  // device tables match tab
+  ddl::Item* d_items = nullptr;
+  ddl::Segment* d_segs = nullptr;
+  uint8_t* d_orders = nullptr;
+  ddl::Xfer* d_xfers = nullptr;
+  uint32_t* d_err = nullptr;
+  cudaStream_t side = nullptr;
+  std::vector<cudaEvent_t> ev_ready;
+  cudaEvent_t ev_done = nullptr;
+  uint64_t launches = 0;
+  // overlap with back-propagation
+  bool ov_active = false;
+  std::vector<void*> ov_bufs;
+  float ov_scale = 1.f;
+  std::vector<char> ov_issued;
+  // last rank-pointer set that passed the device-pointer check
+  std::vector<void*> checked;
+};
+
+namespace {
+
+using ddl::Spec;
+
+ddl_status_t rebuild(ddl_plan* p) {
+  ddl::Tables t;
+  if (!ddl::build_tables(p->spec, p->spec.mode == ddl::kStepwise, &t)) return DDL_ERR_OOM;
+  if (t.items.size() > 0xFFFFFFFFull || t.xfers.size() > 0xFFFFFFFFull) return DDL_ERR_UNSUPPORTED;
+  p->tab = std::move(t);
+  p->dev_current = false;
+  return DDL_OK;
+}
+
+void free_device_tables(ddl_plan* p) {
+  cudaFree(p->d_items);
+  cudaFree(p->d_segs);
+  cudaFree(p->d_orders);
+  cudaFree(p->d_xfers);
+  p->d_items = nullptr;
+  p->d_segs = nullptr;
+  p->d_orders = nullptr;
+  p->d_xfers = nullptr;
+}
+
+template <typename T>
+cudaError_t upload(T** dst, const std::vector<T>& v) {
+  if (v.empty()) return cudaSuccess;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(dst), v.size() * sizeof(T));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpy(*dst, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice);
+}
+
+ddl_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DDL_OK;
+  cudaGetLastError();  // clear a non-sticky error so later calls start clean
+  return e == cudaErrorMemoryAllocation ? DDL_ERR_OOM : DDL_ERR_CUDA;
+}
+
+// Binds the plan to the current device and makes its device tables current.
+ddl_status_t ensure_device(ddl_plan* p) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (p->device >= 0 && p->device != dev) return DDL_ERR_INVALID_ARG;
+  if (p->device < 0) {
+    p->device = dev;
+    e = cudaMalloc(reinterpret_cast<void**>(&p->d_err), sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(p->d_err, 0, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_done, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  if (!p->dev_current) {
+    free_device_tables(p);
+    e = upload(&p->d_items, p->tab.items);
+    if (e == cudaSuccess) e = upload(&p->d_segs, p->tab.segs);
+    if (e == cudaSuccess) e = upload(&p->d_orders, p->tab.orders);
+    if (e == cudaSuccess) e = upload(&p->d_xfers, p->tab.xfers);
+    if (e != cudaSuccess) {
+      free_device_tables(p);
+      return cuda_status(e);
+    }
+    const size_t nb = p->tab.buckets.size();
+    while (p->ev_ready.size() < nb) {
+      cudaEvent_t ev;
+      e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+      if (e != cudaSuccess) return cuda_status(e);
+      p->ev_ready.push_back(ev);
+    }
+    p->dev_current = true;
+  }
+  return DDL_OK;
+}
+
+// Checks the P rank pointers: non-null, distinct, non-overlapping, and (once
+// per new pointer set) device-accessible memory.  *aligned = all 16-byte aligned.
+ddl_status_t check_bufs(ddl_plan* p, void* const* bufs, bool device_check, bool* aligned) {
+  if (!bufs) return DDL_ERR_INVALID_ARG;
+  const int P = p->spec.P;
+  const uint64_t bytes = p->spec.N * (uint64_t)p->spec.esize;
+  std::vector<uintptr_t> a(P);
+  bool al = true;
+  for (int r = 0; r < P; ++r) {
+    if (!bufs[r]) return DDL_ERR_INVALID_ARG;
+    a[r] = reinterpret_cast<uintptr_t>(bufs[r]);
+    al = al && (a[r] % 16 == 0);
+  }
+  std::sort(a.begin(), a.end());
+  for (int r = 0; r + 1 < P; ++r)
+    if (a[r] + bytes > a[r + 1] || a[r] + bytes < a[r]) return DDL_ERR_INVALID_ARG;
+  *aligned = al;
+  if (!device_check) return DDL_OK;
+  if (p->checked.size() == (size_t)P && std::equal(p->checked.begin(), p->checked.end(), bufs)) return DDL_OK;
+  for (int r = 0; r < P; ++r) {
+    cudaPointerAttributes at;
+    const cudaError_t e = cudaPointerGetAttributes(&at, bufs[r]);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return DDL_ERR_INVALID_ARG;
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return DDL_ERR_INVALID_ARG;
+    if (at.type == cudaMemoryTypeDevice && at.device != p->device) return DDL_ERR_INVALID_ARG;
+  }
+  p->checked.assign(bufs, bufs + P);
+  return DDL_OK;
+}
+
+ddl_status_t run_bucket(ddl_plan* p, int b, void* const* bufs, bool aligned, float scale, cudaStream_t s) {
+  const ddl::Bucket& bk = p->tab.buckets[b];
+  const bool f16 = p->spec.esize == 2;
+  if (p->spec.mode == ddl::kStepwise) {
+    ddl::StepParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.xfers = p->d_xfers;
+    sp.err = p->d_err;
+    sp.P = p->spec.P;
+    sp.scale = scale;
+    sp.vector_ok = aligned ? 1 : 0;
+    for (int r = 0; r < p->spec.P; ++r) sp.bufs[r] = bufs[r];
+    for (uint32_t st = bk.step_begin; st < bk.step_end; ++st) {
+      const ddl::Step& step = p->tab.steps[st];
+      sp.xfer0 = step.xfer_begin;
+      const cudaError_t e = ddl::launch_step(sp, step.xfer_end - step.xfer_begin, step.max_len, f16, s);
+      if (e != cudaSuccess) return cuda_status(e);
+      ++p->launches;
+    }
+    return DDL_OK;
+  }
+  ddl::FoldParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.items = p->d_items;
+  fp.segs = p->d_segs;
+  fp.orders = p->d_orders;
+  fp.err = p->d_err;
+  fp.item0 = bk.item_begin;
+  fp.n_segs = (uint32_t)p->tab.segs.size();
+  fp.n_orders = (uint32_t)p->tab.orders.size();
+  fp.P = p->spec.P;
+  fp.scale = scale;
+  fp.round_hops = (f16 && p->spec.mode == ddl::kFused) ? 1 : 0;
+  fp.vector_ok = aligned ? 1 : 0;
+  for (int r = 0; r < p->spec.P; ++r) fp.bufs[r] = bufs[r];
+  const int variant = p->kernel == DDL_KERNEL_BULK ? ddl::kVarBulk : ddl::kVarLdg;
+  const uint32_t n = bk.item_end - bk.item_begin;
+  if (n == 0) return DDL_OK;
+  const cudaError_t e = ddl::launch_fold(fp, n, f16, variant, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  ++p->launches;
+  return DDL_OK;
+}
+
+ddl_status_t prepare(ddl_plan* p, void* const* bufs, bool* aligned) {
+  if (!p) return DDL_ERR_INVALID_ARG;
+  bool al = false;
+  ddl_status_t st = check_bufs(p, bufs, false, &al);
+  if (st != DDL_OK) return st;
+  st = ensure_device(p);
+  if (st != DDL_OK) return st;
+  st = check_bufs(p, bufs, true, &al);
+  if (st != DDL_OK) return st;
+  *aligned = al;
+  return DDL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ddl_status_t ddl_plan_create(int P, size_t N, ddl_dtype_t dtype, ddl_topology_t topo, size_t bucket_bytes,
+                             ddl_plan_t* out) {
+  if (!out) return DDL_ERR_INVALID_ARG;
+  *out = nullptr;
+  Spec s;
+  s.P = P;
+  s.N = N;
+  s.esize = dtype == DDL_FP16 ? 2 : (dtype == DDL_FP32 ? 4 : 0);
+  s.topo = topo.kind;
+  s.k = topo.kind == DDL_MULTIRING ? topo.k : 1;
+  s.X = topo.kind == DDL_TORUS ? topo.X : 0;
+  s.Y = topo.kind == DDL_TORUS ? topo.Y : 0;
+  s.bucket_bytes = bucket_bytes;
+  bool unsupported = false;
+  const std::string why = ddl::validate(s, &unsupported);
+  if (!why.empty()) return unsupported ? DDL_ERR_UNSUPPORTED : DDL_ERR_INVALID_ARG;
+  ddl_plan* p = new (std::nothrow) ddl_plan();
+  if (!p) return DDL_ERR_OOM;
+  p->spec = s;
+  const ddl_status_t st = rebuild(p);
+  if (st != DDL_OK) {
+    delete p;
+    return st;
+  }
+  *out = p;
+  return DDL_OK;
+}
+
+ddl_status_t ddl_plan_set_layers(ddl_plan_t p, int n_tensors, const size_t* numel) {
+  if (!p || n_tensors < 0 || (n_tensors > 0 && !numel) || p->ov_active) return DDL_ERR_INVALID_ARG;
+  Spec s = p->spec;
+  s.layers.assign(numel, numel + n_tensors);
+  bool unsupported = false;
+  const std::string why = ddl::validate(s, &unsupported);
+  if (!why.empty()) return unsupported ? DDL_ERR_UNSUPPORTED : DDL_ERR_INVALID_ARG;
+  const Spec old = p->spec;
+  p->spec = s;
+  const ddl_status_t st = rebuild(p);
+  if (st != DDL_OK) p->spec = old;
+  return st;
+}
+
+ddl_status_t ddl_plan_set_mode(ddl_plan_t p, ddl_mode_t mode) {
+  if (!p || p->ov_active || mode < DDL_MODE_FUSED || mode > DDL_MODE_RANKORDER) return DDL_ERR_INVALID_ARG;
+  if ((int)mode == p->spec.mode) return DDL_OK;
+  const Spec old = p->spec;
+  p->spec.mode = (int)mode;
+  const ddl_status_t st = rebuild(p);
+  if (st != DDL_OK) {
+    p->spec = old;
+    rebuild(p);
+  }
+  return st;
+}
+
+ddl_status_t ddl_plan_set_kernel(ddl_plan_t p, ddl_kernel_t k) {
+  if (!p || k < DDL_KERNEL_AUTO || k > DDL_KERNEL_BULK) return DDL_ERR_INVALID_ARG;
+  p->kernel = (int)k;
+  return DDL_OK;
+}
+
+ddl_status_t ddl_allreduce(ddl_plan_t p, void* const* bufs, float scale, void* stream) {
+  bool aligned = false;
+  ddl_status_t st = prepare(p, bufs, &aligned);
+  if (st != DDL_OK) return st;
+  if (p->ov_active) return DDL_ERR_INVALID_ARG;
+  for (int b = 0; b < (int)p->tab.buckets.size(); ++b) {
+    st = run_bucket(p, b, bufs, aligned, scale, static_cast<cudaStream_t>(stream));
+    if (st != DDL_OK) return st;
+  }
+  return DDL_OK;
+}
+
+ddl_status_t ddl_allreduce_bucket(ddl_plan_t p, int bucket, void* const* bufs, float scale, void* stream) {
+  if (!p || bucket < 0 || bucket >= (int)p->tab.buckets.size()) return DDL_ERR_INVALID_ARG;
+  bool aligned = false;
+  const ddl_status_t st = prepare(p, bufs, &aligned);
+  if (st != DDL_OK) return st;
+  return run_bucket(p, bucket, bufs, aligned, scale, static_cast<cudaStream_t>(stream));
+}
+
+ddl_status_t ddl_allreduce_host(ddl_plan_t p, void* const* host_bufs, void* const* dev_bufs, float scale,
+                                void* stream) {
+  if (!p || !host_bufs) return DDL_ERR_INVALID_ARG;
+  for (int r = 0; r < p->spec.P; ++r)
+    if (!host_bufs[r]) return DDL_ERR_INVALID_ARG;
+  bool aligned = false;
+  ddl_status_t st = prepare(p, dev_bufs, &aligned);
+  if (st != DDL_OK) return st;
+  if (p->ov_active) return DDL_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = p->spec.N * (size_t)p->spec.esize;
+  for (int r = 0; r < p->spec.P; ++r) {
+    const cudaError_t e = cudaMemcpyAsync(dev_bufs[r], host_bufs[r], bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  for (int b = 0; b < (int)p->tab.buckets.size(); ++b) {
+    st = run_bucket(p, b, dev_bufs, aligned, scale, s);
+    if (st != DDL_OK) return st;
+  }
+  for (int r = 0; r < p->spec.P; ++r) {
+    const cudaError_t e = cudaMemcpyAsync(host_bufs[r], dev_bufs[r], bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return DDL_OK;
+}
+
+ddl_status_t ddl_overlap_begin(ddl_plan_t p, void* const* bufs, float scale, void* stream) {
+  (void)stream;
+  bool aligned = false;
+  if (p && p->ov_active) return DDL_ERR_INVALID_ARG;
+  const ddl_status_t st = prepare(p, bufs, &aligned);
+  if (st != DDL_OK) return st;
+  p->ov_bufs.assign(bufs, bufs + p->spec.P);
+  p->ov_scale = scale;
+  p->ov_issued.assign(p->tab.buckets.size(), 0);
+  p->ov_active = true;
+  return DDL_OK;
+}
+
+ddl_status_t ddl_bucket_ready(ddl_plan_t p, int bucket, void* stream) {
+  if (!p || !p->ov_active || bucket < 0 || bucket >= (int)p->tab.buckets.size() || p->ov_issued[bucket])
+    return DDL_ERR_INVALID_ARG;
+  bool aligned = false;
+  ddl_status_t st = prepare(p, p->ov_bufs.data(), &aligned);
+  if (st != DDL_OK) return st;
+  cudaError_t e = cudaEventRecord(p->ev_ready[bucket], static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(p->side, p->ev_ready[bucket], 0);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->ov_issued[bucket] = 1;
+  return run_bucket(p, bucket, p->ov_bufs.data(), aligned, p->ov_scale, p->side);
+}
+
+ddl_status_t ddl_overlap_end(ddl_plan_t p, void* stream) {
+  if (!p || !p->ov_active) return DDL_ERR_INVALID_ARG;
+  p->ov_active = false;
+  cudaError_t e = cudaEventRecord(p->ev_done, p->side);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), p->ev_done, 0);
+  return cuda_status(e);
+}
+
+ddl_status_t ddl_plan_num_buckets(ddl_plan_t p, int* n) {
+  if (!p || !n) return DDL_ERR_INVALID_ARG;
+  *n = (int)p->tab.buckets.size();
+  return DDL_OK;
+}
+
+ddl_status_t ddl_plan_bucket_range(ddl_plan_t p, int b, size_t* begin, size_t* end) {
+  if (!p || !begin || !end || b < 0 || b >= (int)p->tab.buckets.size()) return DDL_ERR_INVALID_ARG;
+  *begin = p->tab.buckets[b].lo;
+  *end = p->tab.buckets[b].hi;
+  return DDL_OK;
+}
+
+ddl_status_t ddl_plan_traffic(ddl_plan_t p, uint64_t* moved, uint64_t* steps) {
+  if (!p || !moved || !steps) return DDL_ERR_INVALID_ARG;
+  *moved = p->tab.moved;
+  *steps = p->tab.nsteps;
+  return DDL_OK;
+}
+
+ddl_status_t ddl_plan_fold_order(ddl_plan_t p, size_t i, int32_t* order, int32_t* inner, int32_t* groups) {
+  if (!p || !order || !inner || !groups) return DDL_ERR_INVALID_ARG;
+  if (p->spec.mode == ddl::kStepwise) return DDL_ERR_UNSUPPORTED;
+  return ddl::fold_order_of(p->spec, p->tab, i, order, inner, groups) ? DDL_OK : DDL_ERR_INVALID_ARG;
+}
+
+ddl_status_t ddl_plan_launches(ddl_plan_t p, uint64_t* n) {
+  if (!p || !n) return DDL_ERR_INVALID_ARG;
+  *n = p->launches;
+  return DDL_OK;
+}
+
+ddl_status_t ddl_plan_check(ddl_plan_t p) {
+  if (!p) return DDL_ERR_INVALID_ARG;
+  if (p->device < 0) return DDL_OK;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_status(e);
+  uint32_t w = 0;
+  e = cudaMemcpy(&w, p->d_err, sizeof(w), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (w == 0) return DDL_OK;
+  cudaMemset(p->d_err, 0, sizeof(uint32_t));
+  return DDL_ERR_DEVICE_CHECK;
+}
+
+const char* ddl_status_string(ddl_status_t s) {
+  switch (s) {
+    case DDL_OK: return "DDL_OK";
+    case DDL_ERR_INVALID_ARG: return "DDL_ERR_INVALID_ARG: invalid argument";
+    case DDL_ERR_UNSUPPORTED: return "DDL_ERR_UNSUPPORTED: request outside what the library builds";
+    case DDL_ERR_OOM: return "DDL_ERR_OOM: allocation failed";
+    case DDL_ERR_CUDA: return "DDL_ERR_CUDA: a CUDA call or kernel launch failed";
+    case DDL_ERR_DEVICE_CHECK: return "DDL_ERR_DEVICE_CHECK: a kernel's own check failed";
+  }
+  return "unknown ddl_status_t";
+}
+
+ddl_status_t ddl_plan_destroy(ddl_plan_t p) {
+  if (!p) return DDL_OK;
+  if (p->device >= 0) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device) cudaSetDevice(p->device);
+    if (p->side) cudaStreamSynchronize(p->side);
+    free_device_tables(p);
+    cudaFree(p->d_err);
+    for (cudaEvent_t ev : p->ev_ready) cudaEventDestroy(ev);
+    if (p->ev_done) cudaEventDestroy(p->ev_done);
+    if (p->side) cudaStreamDestroy(p->side);
+    if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
+  }
+  delete p;
+  return DDL_OK;
+}
+
+}  // extern "C"

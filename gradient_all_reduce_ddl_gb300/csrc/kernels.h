@@ -1,0 +1,52 @@
+// kernels.h -- launch records of the all-reduce kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "plan.h"
+
+namespace ddl {
+
+// Error word bits written by kernels (read back by ddl_plan_check).
+enum : uint32_t {
+  kErrBadItem = 1u,      // a work item points outside the segment table
+  kErrBadOrder = 2u,     // a segment's group shape does not cover P ranks
+  kErrWaitTimeout = 4u,  // a bounded wait on an mbarrier ran out
+  kErrBadXfer = 8u       // a message names a rank outside 0..P-1
+};
+
+struct FoldParams {
+  const Item* items;
+  const Segment* segs;
+  const uint8_t* orders;
+  uint32_t* err;
+  uint32_t item0;      // first item of this launch
+  uint32_t n_segs;
+  uint32_t n_orders;
+  int32_t P;
+  float scale;
+  int32_t round_hops;  // binary16 storage: round every intermediate result
+  int32_t vector_ok;   // every rank pointer is 16-byte aligned
+  int32_t pad;
+  void* bufs[kMaxP];   // rank r's buffer
+};
+
+struct StepParams {
+  const Xfer* xfers;
+  uint32_t* err;
+  uint32_t xfer0;
+  int32_t P;
+  float scale;
+  int32_t vector_ok;
+  void* bufs[kMaxP];
+};
+
+// Variants of the fused pass.
+enum FoldVariant : int { kVarLdg = 1, kVarBulk = 2 };
+
+cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream);
+cudaError_t launch_step(const StepParams& p, uint32_t n_xfers, uint64_t max_len, bool f16, cudaStream_t stream);
+
+}  // namespace ddl

@@ -1,0 +1,322 @@
+// plan.cpp -- builds the tables that drive the all-reduce kernels.
+//
+// The schedules (sources by page title and section):
+//  * ring: Baidu ring-allreduce write-up (final page), "总结" -- a chunked
+//    reduce-scatter, then an all-gather, around a ring;
+//  * multi-ring: "[论文解读] PowerAI DDL", abstract and "提出的方法" -- several
+//    rings with different rank orders share the gradient;
+//  * 2D-torus: "索尼发布新的方法，在ImageNet数据集上224秒内成功训练了ResNet-50",
+//    "2D-Torus All-reduce", Fig. 1 / Fig. 2 -- horizontal reduce-scatter,
+//    vertical all-reduce, horizontal all-gather;
+//  * buckets in reverse-layer order: Baidu write-up, opening paragraphs.
+//
+// Fused mode turns each schedule into a per-element fold order: in a ring
+// whose position t sends to t+1 and, at reduce-scatter step s, sends chunk
+// (t - s) mod m, chunk c is first sent by position c and ends, fully reduced,
+// at position c - 1; its value is the left fold of positions c, c+1, ...,
+// c+m-1.  The torus nests two such folds: row chunk c is folded along each
+// row from column c on, and its sub-chunk d is folded down the column from
+// row d on.  Every element of one (bucket, slice, chunk) run shares one order,
+// so the tables list runs ("segments") and tile-sized work items over them.
+#include "plan.h"
+
+#include <algorithm>
+#include <new>
+#include <numeric>
+
+namespace ddl {
+namespace {
+
+// Split of n elements into m parts: part i has n/m + (i < n%m) elements and
+// starts at i*(n/m) + min(i, n%m).
+inline uint64_t part_len(uint64_t n, uint64_t m, uint64_t i) { return n / m + (i < n % m ? 1 : 0); }
+inline uint64_t part_lo(uint64_t n, uint64_t m, uint64_t i) { return i * (n / m) + std::min(i, n % m); }
+
+int gcd_int(int a, int b) {
+  while (b) {
+    const int r = a % b;
+    a = b;
+    b = r;
+  }
+  return a;
+}
+
+void make_buckets(const Spec& s, std::vector<Bucket>* out) {
+  out->clear();
+  auto push = [&](uint64_t lo, uint64_t hi) {
+    Bucket b{};
+    b.lo = lo;
+    b.hi = hi;
+    out->push_back(b);
+  };
+  if (s.bucket_bytes == 0) {
+    push(0, s.N);
+    return;
+  }
+  if (s.layers.empty()) {
+    const uint64_t per = s.bucket_bytes / (uint64_t)s.esize;
+    uint64_t hi = s.N;
+    while (hi > 0) {
+      const uint64_t lo = hi > per ? hi - per : 0;
+      push(lo, hi);
+      hi = lo;
+    }
+    return;
+  }
+  // tensors sit in forward order at increasing addresses; walk them backwards
+  uint64_t top = s.N, cursor = s.N, bytes = 0;
+  for (size_t i = s.layers.size(); i-- > 0;) {
+    cursor -= s.layers[i];
+    bytes += s.layers[i] * (uint64_t)s.esize;
+    if (bytes >= s.bucket_bytes) {
+      push(cursor, top);
+      top = cursor;
+      bytes = 0;
+    }
+  }
+  if (top > 0) push(0, top);
+}
+
+struct Builder {
+  const Spec& s;
+  Tables* t;
+  bool with_steps;
+  std::vector<int> mult;
+
+  void add_segment(uint64_t lo, uint64_t len, const std::vector<int>& order, int inner, int groups) {
+    if (len == 0) return;
+    Segment g;
+    g.order_off = (uint32_t)t->orders.size();
+    g.inner = (uint16_t)inner;
+    g.groups = (uint16_t)groups;
+    for (int r : order) t->orders.push_back((uint8_t)r);
+    const uint32_t seg = (uint32_t)t->segs.size();
+    t->segs.push_back(g);
+    const uint64_t tile = (uint64_t)kTileBytes / (uint64_t)s.esize;
+    for (uint64_t a = lo, end = lo + len; a < end;) {
+      const uint64_t next = std::min(end, (a / tile + 1) * tile);
+      t->items.push_back(Item{a, (uint32_t)(next - a), seg});
+      a = next;
+    }
+  }
+
+  void fused_bucket(const Bucket& b) {
+    const int P = s.P;
+    const uint64_t n = b.hi - b.lo;
+    std::vector<int> order(P);
+    if (s.mode == kRankOrder) {
+      std::iota(order.begin(), order.end(), 0);
+      add_segment(b.lo, n, order, P, 1);
+      return;
+    }
+    if (s.topo == kRing || s.topo == kMultiRing) {
+      const int k = s.topo == kRing ? 1 : s.k;
+      for (int j = 0; j < k; ++j) {
+        const uint64_t slo = b.lo + part_lo(n, k, j), sn = part_len(n, k, j);
+        const int m = s.topo == kRing ? 1 : mult[j];
+        for (int c = 0; c < P; ++c) {
+          for (int t2 = 0; t2 < P; ++t2) order[t2] = (int)((int64_t)((c + t2) % P) * m % P);
+          add_segment(slo + part_lo(sn, P, c), part_len(sn, P, c), order, P, 1);
+        }
+      }
+      return;
+    }
+    const int X = s.X, Y = s.Y;
+    for (int c = 0; c < X; ++c) {
+      const uint64_t clo = b.lo + part_lo(n, X, c), cn = part_len(n, X, c);
+      for (int d = 0; d < Y; ++d) {
+        for (int g = 0; g < Y; ++g)
+          for (int h = 0; h < X; ++h) order[g * X + h] = ((d + g) % Y) * X + (c + h) % X;
+        add_segment(clo + part_lo(cn, Y, d), part_len(cn, Y, d), order, X, Y);
+      }
+    }
+  }
+
+  // ---- message lists of the step-by-step schedule ----
+  std::vector<Xfer> cur;
+
+  void msg(uint64_t lo, uint64_t len, int src, int dst, uint32_t op) {
+    t->moved += (op == kScaleOnly) ? 0 : len;
+    if (!with_steps) return;
+    Xfer x{};
+    x.lo = lo;
+    x.len = len;
+    x.src = (uint16_t)src;
+    x.dst = (uint16_t)dst;
+    x.op = op;
+    cur.push_back(x);
+  }
+  // ring positions `ring`, elements [lo, lo+n), reduce-scatter step s
+  void rs(const std::vector<int>& ring, uint64_t lo, uint64_t n, int step, bool owner_final) {
+    const int m = (int)ring.size();
+    for (int p = 0; p < m; ++p) {
+      const int c = ((p - step) % m + m) % m;
+      const bool fin = owner_final && step == m - 2;
+      msg(lo + part_lo(n, m, c), part_len(n, m, c), ring[p], ring[(p + 1) % m], fin ? kAddFinal : kAddHop);
+    }
+  }
+  void ag(const std::vector<int>& ring, uint64_t lo, uint64_t n, int step) {
+    const int m = (int)ring.size();
+    for (int p = 0; p < m; ++p) {
+      const int c = ((p + 1 - step) % m + m) % m;
+      msg(lo + part_lo(n, m, c), part_len(n, m, c), ring[p], ring[(p + 1) % m], kCopy);
+    }
+  }
+  void close_step(bool communication) {
+    if (communication) ++t->nsteps;
+    if (!with_steps) return;
+    Step st{};
+    st.xfer_begin = (uint32_t)t->xfers.size();
+    uint64_t mx = 0;
+    for (const Xfer& x : cur) {
+      if (x.len == 0) continue;
+      t->xfers.push_back(x);
+      mx = std::max<uint64_t>(mx, x.len);
+    }
+    st.xfer_end = (uint32_t)t->xfers.size();
+    st.max_len = mx;
+    cur.clear();
+    if (st.xfer_end > st.xfer_begin) t->steps.push_back(st);
+  }
+
+  void step_bucket(const Bucket& b) {
+    const int P = s.P;
+    const uint64_t n = b.hi - b.lo;
+    if (P == 1) {  // a ring of one: the owner scales and nothing moves
+      msg(b.lo, n, 0, 0, kScaleOnly);
+      close_step(false);
+      return;
+    }
+    if (s.topo == kRing || s.topo == kMultiRing) {
+      const int k = s.topo == kRing ? 1 : s.k;
+      std::vector<std::vector<int>> rings(k, std::vector<int>(P));
+      for (int j = 0; j < k; ++j)
+        for (int p = 0; p < P; ++p) rings[j][p] = (int)((int64_t)p * (s.topo == kRing ? 1 : mult[j]) % P);
+      for (int st = 0; st < P - 1; ++st) {
+        for (int j = 0; j < k; ++j) rs(rings[j], b.lo + part_lo(n, k, j), part_len(n, k, j), st, true);
+        close_step(true);
+      }
+      for (int st = 0; st < P - 1; ++st) {
+        for (int j = 0; j < k; ++j) ag(rings[j], b.lo + part_lo(n, k, j), part_len(n, k, j), st);
+        close_step(true);
+      }
+      return;
+    }
+    const int X = s.X, Y = s.Y;
+    std::vector<std::vector<int>> row(Y, std::vector<int>(X)), col(X, std::vector<int>(Y));
+    for (int y = 0; y < Y; ++y)
+      for (int x = 0; x < X; ++x) row[y][x] = y * X + x;
+    for (int c = 0; c < X; ++c)
+      for (int y = 0; y < Y; ++y) col[c][y] = y * X + (c + X - 1) % X;  // row chunk c ends at column c-1
+    for (int st = 0; st < X - 1; ++st) {
+      for (int y = 0; y < Y; ++y) rs(row[y], b.lo, n, st, Y == 1);
+      close_step(true);
+    }
+    for (int st = 0; st < Y - 1; ++st) {
+      for (int c = 0; c < X; ++c) rs(col[c], b.lo + part_lo(n, X, c), part_len(n, X, c), st, true);
+      close_step(true);
+    }
+    for (int st = 0; st < Y - 1; ++st) {
+      for (int c = 0; c < X; ++c) ag(col[c], b.lo + part_lo(n, X, c), part_len(n, X, c), st);
+      close_step(true);
+    }
+    for (int st = 0; st < X - 1; ++st) {
+      for (int y = 0; y < Y; ++y) ag(row[y], b.lo, n, st);
+      close_step(true);
+    }
+  }
+};
+
+}  // namespace
+
+bool ring_multipliers(int P, int k, std::vector<int>* out) {
+  out->clear();
+  if (P == 1) {
+    out->push_back(1);
+    return k == 1;
+  }
+  for (int c = 1; c < P && (int)out->size() < k; ++c)
+    if (gcd_int(c, P) == 1) out->push_back(c);
+  return (int)out->size() == k;
+}
+
+std::string validate(const Spec& s, bool* unsupported) {
+  *unsupported = false;
+  if (s.P < 1) return "P must be >= 1";
+  if (s.P > kMaxP) {
+    *unsupported = true;
+    return "P > 256 is not supported";
+  }
+  if (s.N < 1) return "N must be >= 1";
+  if (s.esize != 4 && s.esize != 2) return "dtype must be DDL_FP32 or DDL_FP16";
+  if (s.mode < kFused || s.mode > kRankOrder) return "unknown mode";
+  if (s.topo == kMultiRing) {
+    std::vector<int> m;
+    if (s.k < 1) return "multi-ring needs k >= 1";
+    if (!ring_multipliers(s.P, s.k, &m)) {
+      *unsupported = true;
+      return "multi-ring k exceeds the number of distinct rank orders t*s mod P (phi(P))";
+    }
+  } else if (s.topo == kTorus) {
+    if (s.X < 1 || s.Y < 1 || (int64_t)s.X * s.Y != s.P) return "torus needs X * Y == P";
+  } else if (s.topo != kRing) {
+    return "unknown topology kind";
+  }
+  if (s.bucket_bytes != 0 && s.bucket_bytes < (uint64_t)s.esize) return "bucket_bytes smaller than one element";
+  if (!s.layers.empty()) {
+    uint64_t sum = 0;
+    for (uint64_t v : s.layers) {
+      if (v == 0) return "a layer has zero elements";
+      sum += v;
+    }
+    if (sum != s.N) return "layer sizes do not sum to N";
+  }
+  // work-item indices are 32-bit: up to 2^40 bytes per rank
+  if (s.N * (uint64_t)s.esize > (1ull << 40)) {
+    *unsupported = true;
+    return "more than 2^40 bytes per rank";
+  }
+  return "";
+}
+
+bool build_tables(const Spec& s, bool with_steps, Tables* t) {
+  try {
+    *t = Tables();
+    make_buckets(s, &t->buckets);
+    Builder bld{s, t, with_steps, {}};
+    if (s.topo == kMultiRing) ring_multipliers(s.P, s.k, &bld.mult);
+    for (Bucket& b : t->buckets) {
+      b.item_begin = (uint32_t)t->items.size();
+      if (s.mode != kStepwise) bld.fused_bucket(b);
+      b.item_end = (uint32_t)t->items.size();
+      b.step_begin = (uint32_t)t->steps.size();
+      bld.step_bucket(b);
+      b.step_end = (uint32_t)t->steps.size();
+    }
+    return true;
+  } catch (const std::bad_alloc&) {
+    *t = Tables();
+    return false;
+  }
+}
+
+bool fold_order_of(const Spec& s, const Tables& t, uint64_t i, int32_t* order, int32_t* inner, int32_t* groups) {
+  if (i >= s.N || s.mode == kStepwise) return false;
+  // items are sorted by element within each bucket; buckets run downwards
+  for (const Bucket& b : t.buckets) {
+    if (i < b.lo || i >= b.hi) continue;
+    auto first = t.items.begin() + b.item_begin, last = t.items.begin() + b.item_end;
+    auto it = std::upper_bound(first, last, i, [](uint64_t v, const Item& x) { return v < x.begin; });
+    if (it == first) return false;
+    --it;
+    if (i >= it->begin + it->len) return false;
+    const Segment& g = t.segs[it->seg];
+    for (int r = 0; r < s.P; ++r) order[r] = t.orders[g.order_off + r];
+    *inner = g.inner;
+    *groups = g.groups;
+    return true;
+  }
+  return false;
+}
+
+}  // namespace ddl

@@ -1,0 +1,100 @@
+// plan.h -- host-side tables of an all-reduce plan, and the records the
+// kernels read.  Host code only builds them; no CUDA calls here.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+namespace ddl {
+
+constexpr int kMaxP = 256;          // rank orders are stored as bytes
+constexpr int kTileBytes = 8192;    // bytes per rank in one fused work item
+
+// One contiguous run of elements whose fold order is the same.  The ranks are
+// added in the order orders[order_off .. order_off+P), as `groups` groups of
+// `inner` consecutive ranks: each group is left-folded, then the group totals
+// are left-folded.  Ring and multi-ring: groups = 1.  Torus: inner = X
+// (a row, from column c on), groups = Y (rows from row d on).
+struct Segment {
+  uint32_t order_off;
+  uint16_t inner;
+  uint16_t groups;
+};
+
+// One CTA's work in the fused pass: elements [begin, begin + len) of segment
+// `seg`.  Items never cross a segment edge or a kTileBytes-aligned boundary.
+struct Item {
+  uint64_t begin;
+  uint32_t len;
+  uint32_t seg;
+};
+
+// One message of one communication step (stepwise mode).
+enum XferOp : uint32_t {
+  kAddHop = 0,    // dst += src; the result travels again (rounded to storage)
+  kAddFinal = 1,  // dst = (src + dst) * scale; the owner's last add
+  kCopy = 2,      // dst = src (all-gather)
+  kScaleOnly = 3  // dst = dst * scale (a ring of one: the owner has no add)
+};
+
+struct Xfer {
+  uint64_t lo;
+  uint64_t len;
+  uint16_t src;
+  uint16_t dst;
+  uint32_t op;
+};
+
+struct Step {
+  uint32_t xfer_begin, xfer_end;
+  uint64_t max_len;
+};
+
+struct Bucket {
+  uint64_t lo, hi;
+  uint32_t item_begin, item_end;  // fused / rank-order items
+  uint32_t step_begin, step_end;  // stepwise steps
+};
+
+enum Topo : int32_t { kRing = 0, kMultiRing = 1, kTorus = 2 };
+enum Mode : int32_t { kFused = 0, kStepwise = 1, kRankOrder = 2 };
+
+struct Spec {
+  int P = 0;
+  uint64_t N = 0;
+  int esize = 4;      // 4 (binary32) or 2 (binary16)
+  int topo = kRing;
+  int k = 1, X = 0, Y = 0;
+  uint64_t bucket_bytes = 0;
+  std::vector<uint64_t> layers;
+  int mode = kFused;
+};
+
+struct Tables {
+  std::vector<Bucket> buckets;
+  std::vector<Segment> segs;
+  std::vector<uint8_t> orders;
+  std::vector<Item> items;
+  std::vector<Xfer> xfers;
+  std::vector<Step> steps;
+  uint64_t moved = 0;   // elements sent over all messages
+  uint64_t nsteps = 0;  // sequential communication steps
+};
+
+// Returns "" if the spec is valid, else a reason.  unsupported is set when the
+// request is valid in principle but outside what this library builds.
+std::string validate(const Spec& s, bool* unsupported);
+
+// The multi-ring multipliers s_0..s_{k-1}; false if fewer than k exist.
+bool ring_multipliers(int P, int k, std::vector<int>* out);
+
+// Builds buckets, the fused (or rank-order) segment and item tables, and the
+// step/message tables (steps only listed when with_steps).  Returns false on
+// allocation failure.
+bool build_tables(const Spec& s, bool with_steps, Tables* t);
+
+// Fold order of element i from the built tables.
+bool fold_order_of(const Spec& s, const Tables& t, uint64_t i, int32_t* order, int32_t* inner, int32_t* groups);
+
+}  // namespace ddl

@@ -1,0 +1,197 @@
+/*
+ * ddl.h -- C ABI of libddl: the synchronous-SGD gradient all-reduce of P
+ * logical data-parallel workers whose gradient buffers all live in the HBM of
+ * one GPU (GB300, sm_103a).
+ *
+ * What the operation is (sources cited by page title and section):
+ *  - Data-parallel training adds one step to every iteration: the workers'
+ *    gradients are averaged with an all-reduce collective ("索尼发布新的方法，
+ *    在ImageNet数据集上224秒内成功训练了ResNet-50", section "2大方法解决不稳定
+ *    问题"; Baidu ring-allreduce write-up, final page, section "总结").
+ *  - Three schedules: the ring all-reduce, a chunked reduce-scatter then an
+ *    all-gather (Baidu write-up, "总结", after Patarasuk & Yuan 2009); the
+ *    multi-ring pattern of "[论文解读] PowerAI DDL" (abstract, "提出的方法"),
+ *    k rings over different rank orders; and the 2D-torus all-reduce of the
+ *    Sony page, section "2D-Torus All-reduce", Fig. 1 and Fig. 2: on an X x Y
+ *    grid, a horizontal reduce-scatter, a vertical all-reduce and a
+ *    horizontal all-gather.
+ *  - FP16 gradient communication (Sony page, section "训练设置").
+ *  - Buckets in reverse-layer order, so the all-reduce of the output layers
+ *    starts while back-propagation still runs (Baidu write-up, opening
+ *    paragraphs of its final page).
+ *
+ * Result contract: after ddl_allreduce every rank buffer holds, bit for bit,
+ * what the schedule computes when run send-by-send with IEEE binary32 adds in
+ * its own order (fp16 mode: binary16 on every hop, binary32 adds, the owner's
+ * last add kept in binary32, multiplied by the scale, rounded once).  The
+ * rules that fix that order (chunk split, ring direction, multi-ring orders,
+ * torus layout, bucket packing) are stated at each call below.
+ *
+ * Conventions for every call:
+ *  - No call aborts or throws; each returns a ddl_status_t.  Argument errors
+ *    are found before any work is queued and leave no side effects.
+ *  - "stream" is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  GPU work is queued on it asynchronously; calls return after
+ *    enqueue.
+ *  - A plan binds to the CUDA device that is current at its first GPU call;
+ *    later GPU calls must be made with that device current.
+ *  - A plan is not thread-safe: do not call into one plan from two host
+ *    threads at once, and do not queue two all-reduces of one plan that may
+ *    run concurrently on the GPU over the same buffers.
+ */
+#ifndef DDL_H_
+#define DDL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DDL_OK = 0,
+  DDL_ERR_INVALID_ARG = 1,  /* bad argument; nothing was queued */
+  DDL_ERR_UNSUPPORTED = 2,  /* valid request this library does not build (e.g. P > 256) */
+  DDL_ERR_OOM = 3,          /* host or device allocation of plan tables failed */
+  DDL_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+  DDL_ERR_DEVICE_CHECK = 5  /* a kernel's own check failed (see ddl_plan_check) */
+} ddl_status_t;
+
+typedef enum {
+  DDL_FP32 = 0, /* binary32 storage and arithmetic */
+  DDL_FP16 = 1  /* binary16 storage and hops, binary32 adds */
+} ddl_dtype_t;
+
+typedef enum { DDL_RING = 0, DDL_MULTIRING = 1, DDL_TORUS = 2 } ddl_topo_kind_t;
+
+/* kind = DDL_RING: k, X, Y ignored.
+ * kind = DDL_MULTIRING: k rings, 1 <= k <= phi(P); ring j uses the rank order
+ *   pi_j(t) = t * s_j mod P, s_j the j-th smallest integer in [1, P) coprime
+ *   to P (s_0 = 1 when P = 1).
+ * kind = DDL_TORUS: X * Y == P; rank r sits at column x = r mod X, row
+ *   y = r / X; rows are the horizontal rings, columns the vertical ones. */
+typedef struct {
+  int32_t kind;
+  int32_t k;
+  int32_t X;
+  int32_t Y;
+} ddl_topology_t;
+
+typedef enum {
+  DDL_MODE_FUSED = 0,     /* one HBM pass per bucket, schedule order (bit-exact) */
+  DDL_MODE_STEPWISE = 1,  /* one kernel per communication step (bit-exact; slow) */
+  DDL_MODE_RANKORDER = 2  /* one HBM pass, ranks added in order 0..P-1 with no
+                             intermediate binary16 rounding; accurate to the
+                             fp64 sum within 1e-6 (fp32) / 2e-3 (fp16)
+                             normwise, but not the schedule's bits */
+} ddl_mode_t;
+
+typedef enum {
+  DDL_KERNEL_AUTO = 0,  /* the library's choice */
+  DDL_KERNEL_LDG = 1,   /* fused pass with 16-byte register loads and stores */
+  DDL_KERNEL_BULK = 2   /* fused pass staged through shared memory by bulk async copies */
+} ddl_kernel_t;
+
+typedef struct ddl_plan* ddl_plan_t;
+
+/* Creates a plan for P rank buffers of N elements each.
+ *  P: 1..256.  N: >= 1 elements per rank.
+ *  bucket_bytes: 0 = the whole buffer is one bucket; otherwise buckets of at
+ *    least this many bytes, taken from the highest addresses down (bucket 0 =
+ *    output layers, issued first).  Without a layer list (see
+ *    ddl_plan_set_layers) bucket b covers elements
+ *    [max(0, N - (b+1)*B), N - b*B), B = bucket_bytes / element size.
+ *  Inside a bucket of n elements, a split into m parts gives part i
+ *  n/m + (i < n%m) elements starting at i*(n/m) + min(i, n%m); the ring uses
+ *  m = P chunks, the multi-ring k slices of P chunks, the torus X row chunks
+ *  of Y sub-chunks.
+ * Host-only: allocates the plan and builds its tables; touches no GPU.
+ * On success *out owns the plan (free with ddl_plan_destroy). */
+ddl_status_t ddl_plan_create(int P, size_t N, ddl_dtype_t dtype, ddl_topology_t topo,
+                             size_t bucket_bytes, ddl_plan_t* out);
+
+/* Optional: the gradient's tensors, numel_fwd_order[0..n_tensors-1] in
+ * forward (input-to-output) order at increasing addresses; they must sum to
+ * N.  Buckets are then packed greedily from the last tensor backwards, a
+ * bucket closing once it holds >= bucket_bytes; the remainder is the last
+ * bucket.  The array is copied.  Host-only. */
+ddl_status_t ddl_plan_set_layers(ddl_plan_t plan, int n_tensors, const size_t* numel_fwd_order);
+
+/* Selects the mode (default DDL_MODE_FUSED).  Host-only. */
+ddl_status_t ddl_plan_set_mode(ddl_plan_t plan, ddl_mode_t mode);
+
+/* Selects the fused kernel variant (default DDL_KERNEL_AUTO).  Results are
+ * identical for every variant.  Host-only. */
+ddl_status_t ddl_plan_set_kernel(ddl_plan_t plan, ddl_kernel_t kernel);
+
+/* All-reduces every bucket, in place, in issue order.
+ *  rank_bufs: host array of P device pointers, rank r's N elements (binary32,
+ *    or binary16 for DDL_FP16).  The buffers must be distinct and must not
+ *    overlap; the caller owns them and keeps them valid until the queued work
+ *    has finished.  Pointers that are not 16-byte aligned are accepted and
+ *    take a slower element-wise path; results do not change.
+ *  scale: binary32 factor applied once per element (1/P gives the mean).
+ * The first call on a device uploads the plan's tables (device memory owned
+ * by the plan) and creates its side stream and events. */
+ddl_status_t ddl_allreduce(ddl_plan_t plan, void* const* rank_bufs, float scale, void* stream);
+
+/* All-reduces bucket b only (0 <= b < ddl_plan_num_buckets). */
+ddl_status_t ddl_allreduce_bucket(ddl_plan_t plan, int bucket, void* const* rank_bufs, float scale,
+                                  void* stream);
+
+/* End-to-end form: copies P host buffers into the P device buffers, runs the
+ * all-reduce, and copies the results back, all queued on stream.
+ *  host_bufs: P host pointers (page-locked for asynchronous copies; pageable
+ *    memory works but the copies then synchronize), N elements each, updated
+ *    in place.  dev_bufs: P device buffers as for ddl_allreduce, owned by the
+ *    caller.  The host buffers must stay valid until the stream reaches the
+ *    end of the queued work. */
+ddl_status_t ddl_allreduce_host(ddl_plan_t plan, void* const* host_bufs, void* const* dev_bufs, float scale,
+                                void* stream);
+
+/* Overlap with back-propagation.  ddl_overlap_begin records the buffers and
+ * scale; each ddl_bucket_ready(b, stream) marks bucket b's gradients complete
+ * at the current point of `stream` (an event), after which the plan's side
+ * stream all-reduces bucket b; ddl_overlap_end makes `stream` wait for every
+ * bucket issued so far.  Each bucket is signalled at most once per
+ * begin/end pair; bucket 0 (output layers) is normally signalled first. */
+ddl_status_t ddl_overlap_begin(ddl_plan_t plan, void* const* rank_bufs, float scale, void* stream);
+ddl_status_t ddl_bucket_ready(ddl_plan_t plan, int bucket, void* stream);
+ddl_status_t ddl_overlap_end(ddl_plan_t plan, void* stream);
+
+/* Bucket table: *n buckets; bucket b covers elements [*begin, *end). */
+ddl_status_t ddl_plan_num_buckets(ddl_plan_t plan, int* n);
+ddl_status_t ddl_plan_bucket_range(ddl_plan_t plan, int bucket, size_t* begin, size_t* end);
+
+/* What the schedule would move between workers: the total number of
+ * elements sent over all messages (2(P-1)N for every schedule) and the number
+ * of sequential communication steps (ring and multi-ring 2(P-1), torus
+ * 2(X-1)+2(Y-1), per bucket).  Host-only. */
+ddl_status_t ddl_plan_traffic(ddl_plan_t plan, uint64_t* elems_moved_total, uint64_t* steps);
+
+/* Introspection: the fold order of element i as the plan's tables hold it:
+ * order[0..P-1] = ranks in the order they are added, *inner = group length
+ * (X for the torus, else P), *groups = Y for the torus, else 1.  Host-only. */
+ddl_status_t ddl_plan_fold_order(ddl_plan_t plan, size_t i, int32_t* order, int32_t* inner, int32_t* groups);
+
+/* Number of kernels this plan has launched since it was created. */
+ddl_status_t ddl_plan_launches(ddl_plan_t plan, uint64_t* n);
+
+/* Waits for the plan's device work and reads its kernels' error word:
+ * DDL_ERR_DEVICE_CHECK if a kernel found a bad table entry or a bounded wait
+ * ran out (the word is then cleared), DDL_OK otherwise. */
+ddl_status_t ddl_plan_check(ddl_plan_t plan);
+
+/* A static string for a status code. */
+const char* ddl_status_string(ddl_status_t status);
+
+/* Frees the plan, its device tables, side stream and events.  Waits for the
+ * plan's side stream first.  NULL is accepted. */
+ddl_status_t ddl_plan_destroy(ddl_plan_t plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DDL_H_ */

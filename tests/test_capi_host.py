@@ -1,0 +1,153 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol, and
+its host-only calls (plan tables, traffic, errors) agree with the oracle.
+No GPU work is done here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ddl():
+    from gradient_all_reduce_ddl_gb300.build import build
+    build()
+    from gradient_all_reduce_ddl_gb300 import ddl as mod
+    return mod
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ddl.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ddl_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(ddl):
+    names = _declared()
+    assert len(names) >= 18
+    lib = ctypes.CDLL(ddl.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(ddl.EXPORTS) == names
+
+
+def test_status_strings(ddl):
+    for s in range(6):
+        assert ddl.ddl_status_string(s).startswith("DDL_")
+    assert "unknown" in ddl.ddl_status_string(99)
+
+
+def _pair(P, N, dtype="f32", topo="ring", k=1, X=0, Y=0, bucket_bytes=0, layers=None, mode="fused"):
+    from gradient_all_reduce_ddl_gb300 import ddl
+    plan = ddl.Plan(P, N, dtype, topo, k=k, X=X, Y=Y, bucket_bytes=bucket_bytes, layers=layers, mode=mode)
+    cfg = oracle.Config(P, N, dtype, topo, k=k, X=X, Y=Y, bucket_bytes=bucket_bytes, layers=layers)
+    return plan, cfg
+
+
+CASES = [
+    dict(P=1, N=5),
+    dict(P=3, N=7),
+    dict(P=5, N=103, bucket_bytes=64),
+    dict(P=7, N=6),
+    dict(P=16, N=1000, topo="multiring", k=2),
+    dict(P=9, N=301, topo="multiring", k=5, bucket_bytes=400),
+    dict(P=4, N=8, topo="torus", X=2, Y=2),
+    dict(P=16, N=999, topo="torus", X=4, Y=4, bucket_bytes=1000),
+    dict(P=12, N=500, topo="torus", X=3, Y=4),
+    dict(P=6, N=50, topo="torus", X=6, Y=1, dtype="f16", bucket_bytes=30),
+    dict(P=6, N=50, topo="torus", X=1, Y=6, layers=[10, 20, 15, 5], bucket_bytes=40),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_tables_match_oracle(ddl, case):
+    """Buckets, traffic, steps and the fold order of every element, from the
+    library's own tables, equal the oracle's."""
+    plan, cfg = _pair(**case)
+    with plan:
+        assert plan.buckets() == oracle.buckets(cfg)
+        assert plan.traffic() == oracle.traffic(cfg)
+        for i in range(cfg.N):
+            o_ord, o_in, o_gr = oracle.fold_order(cfg, i)
+            l_ord, l_in, l_gr = plan.fold_order(i)
+            assert (l_ord, l_in, l_gr) == (o_ord.tolist(), o_in, o_gr), i
+
+
+@pytest.mark.parametrize("name", ["torus4x4_resnet50", "torus8x4_resnet50_f16", "multiring64_resnet101",
+                                  "ring16_lm300m", "torus4x4_lm300m"])
+def test_workload_tables_match_oracle(ddl, name):
+    w = synth.WORKLOADS[name]
+    with ddl.Plan.for_workload(w) as plan:
+        cfg = oracle.Config(w.P, w.N, w.dtype, w.topo, k=w.k, X=w.X, Y=w.Y, bucket_bytes=w.bucket_bytes,
+                            layers=w.layers)
+        assert plan.buckets() == oracle.buckets(cfg)
+        moved, steps = plan.traffic()
+        assert moved == 2 * (w.P - 1) * w.N
+        assert (moved, steps) == oracle.traffic(cfg)
+        rng = np.random.default_rng(0)
+        for i in rng.integers(0, w.N, 300).tolist() + [0, w.N - 1]:
+            o_ord, o_in, o_gr = oracle.fold_order(cfg, i)
+            assert plan.fold_order(i) == (o_ord.tolist(), o_in, o_gr)
+
+
+def test_rankorder_and_stepwise_tables(ddl):
+    plan, cfg = _pair(P=5, N=50, topo="torus", X=5, Y=1, mode="rankorder")
+    with plan:
+        assert plan.fold_order(13) == ([0, 1, 2, 3, 4], 5, 1)
+        assert plan.traffic() == oracle.traffic(cfg)
+    plan, cfg = _pair(P=5, N=50, mode="stepwise")
+    with plan:
+        with pytest.raises(ddl.DDLError):
+            plan.fold_order(0)
+        assert plan.traffic() == oracle.traffic(cfg)
+
+
+def test_invalid_arguments(ddl):
+    E = ddl.DDLError
+    bad = [
+        dict(P=0, N=10), dict(P=4, N=0), dict(P=6, N=10, topo="torus", X=4, Y=2),
+        dict(P=4, N=10, topo="multiring", k=0), dict(P=4, N=10, layers=[3, 3]),
+        dict(P=4, N=10, bucket_bytes=2), dict(P=4, N=10, layers=[5, 0, 5]),
+    ]
+    for c in bad:
+        with pytest.raises(E) as ei:
+            ddl.Plan(**c)
+        assert ei.value.status == ddl.DDL_ERR_INVALID_ARG, c
+    for c in [dict(P=257, N=10), dict(P=16, N=10, topo="multiring", k=9)]:
+        with pytest.raises(E) as ei:
+            ddl.Plan(**c)
+        assert ei.value.status == ddl.DDL_ERR_UNSUPPORTED, c
+    h = ctypes.c_void_p()
+    assert ddl._lib.ddl_plan_create(4, 10, 7, ddl.ddl_topology_t(0, 1, 0, 0), 0, ctypes.byref(h)) == \
+        ddl.DDL_ERR_INVALID_ARG
+    assert ddl._lib.ddl_plan_create(4, 10, 0, ddl.ddl_topology_t(0, 1, 0, 0), 0, None) == ddl.DDL_ERR_INVALID_ARG
+    # calls on a null plan
+    assert ddl._lib.ddl_plan_set_mode(None, 0) == ddl.DDL_ERR_INVALID_ARG
+    assert ddl._lib.ddl_allreduce(None, None, ctypes.c_float(1.0), None) == ddl.DDL_ERR_INVALID_ARG
+    assert ddl._lib.ddl_plan_destroy(None) == ddl.DDL_OK
+    with ddl.Plan(4, 100) as p:
+        # null / duplicate / overlapping rank pointers are refused before any GPU call
+        for ptrs in ([0, 4096, 8192, 12288], [4096, 4096, 8192, 12288], [4096, 4200, 8192, 12288]):
+            arr = (ctypes.c_void_p * 4)(*ptrs)
+            assert ddl._lib.ddl_allreduce(p.handle, arr, ctypes.c_float(1.0), None) == ddl.DDL_ERR_INVALID_ARG
+        assert ddl._lib.ddl_allreduce(p.handle, None, ctypes.c_float(1.0), None) == ddl.DDL_ERR_INVALID_ARG
+        with pytest.raises(E):
+            p.allreduce_bucket(5, [4096 * (i + 1) for i in range(4)], 1.0, stream=0)
+        with pytest.raises(E):
+            p.bucket_ready(0, stream=0)      # no overlap_begin
+        with pytest.raises(E):
+            p.overlap_end(stream=0)
+        with pytest.raises(E):
+            ddl.ddl_plan_set_mode(p.handle, 7)
+        with pytest.raises(E):
+            ddl.ddl_plan_set_layers(p.handle, [50, 49])
+        # a failed set_layers leaves the plan as it was
+        assert p.buckets() == [(0, 100)]
+        ddl.ddl_plan_set_layers(p.handle, [50, 50])
+        assert p.launches == 0

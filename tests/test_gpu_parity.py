@@ -1,0 +1,253 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle.
+
+Schedule-order modes (fused, stepwise) must match the oracle bit for bit;
+the rank-order mode must be within 1e-6 (fp32) / 2e-3 (fp16) normwise of the
+fp64 sum of the stored inputs.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import (device_bufs_from_host, device_bufs_generated, edge_samples, oracle_cfg, to_numpy_bits,
+                      torch_dtype)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def ddl():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    from gradient_all_reduce_ddl_gb300 import ddl as mod
+    return mod
+
+
+DEV = "cuda:0"
+
+
+def _w(P, N, dtype="f32", topo="ring", k=1, X=0, Y=0, bucket_bytes=0, layers=None, dist="normal", sigma=None,
+       scale=None, seed=1):
+    if sigma is None:
+        sigma = 1e-2 if dtype == "f16" else 1e-3
+    if scale is None:
+        scale = float(np.float32(1.0 / P))
+    return synth.Workload(name="t", P=P, N=N, dtype=dtype, topo=topo, k=k, X=X, Y=Y, bucket_bytes=bucket_bytes,
+                          layers=None if layers is None else tuple(layers), scale=scale, dist=dist, sigma=sigma,
+                          seed=seed)
+
+
+def _host_inputs(w):
+    return [w.rank_values(r) for r in range(w.P)]
+
+
+def _check_exact(ddl, w, mode="fused", kernel="auto", misalign=0):
+    host = _host_inputs(w)
+    if misalign:
+        # rank buffers that start `misalign` elements into a larger tensor
+        bufs = []
+        for h in host:
+            big = torch.zeros(w.N + misalign, dtype=torch_dtype(w.dtype), device=DEV)
+            dev = device_bufs_from_host([h], DEV)[0]
+            big[misalign:] = dev
+            bufs.append(big[misalign:])
+    else:
+        bufs = device_bufs_from_host(host, DEV)
+    with ddl.Plan.for_workload(w, mode=mode, kernel=kernel) as plan:
+        plan.allreduce(bufs, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    ref = [h.copy() for h in host]
+    oracle.emulate(oracle_cfg(w), ref, w.scale)
+    for r in range(w.P):
+        got = to_numpy_bits(bufs[r])
+        if not np.array_equal(got, ref[r]):
+            bad = np.nonzero(got != ref[r])[0]
+            raise AssertionError(f"rank {r}: {bad.size} elements differ, first at {bad[:8]}: "
+                                 f"got {got[bad[:4]]} want {ref[r][bad[:4]]}")
+
+
+# Small cases: several 8 KB tiles per rank, ragged tails, every schedule.
+SMALL = [
+    dict(P=4, N=65_536, dist="int1000", scale=1.0),
+    dict(P=1, N=5000),
+    dict(P=2, N=10_001),
+    dict(P=3, N=7),
+    dict(P=5, N=40_003),
+    dict(P=7, N=30_011, bucket_bytes=20_000),
+    dict(P=16, N=70_001, topo="multiring", k=2),
+    dict(P=9, N=50_000, topo="multiring", k=5, bucket_bytes=40_000),
+    dict(P=64, N=20_011, topo="multiring", k=4, bucket_bytes=30_000),
+    dict(P=4, N=8, topo="torus", X=2, Y=2),
+    dict(P=16, N=99_999, topo="torus", X=4, Y=4),
+    dict(P=12, N=40_000, topo="torus", X=3, Y=4, bucket_bytes=50_000),
+    dict(P=32, N=33_333, topo="torus", X=8, Y=4),
+    dict(P=6, N=12_345, topo="torus", X=6, Y=1),
+    dict(P=6, N=12_345, topo="torus", X=1, Y=6),
+    dict(P=200, N=3001, topo="ring"),
+    dict(P=16, N=20_000, layers=[1000, 5000, 3, 7000, 6997], bucket_bytes=20_000),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_fused_matches_oracle(ddl, case, dtype):
+    if dtype == "f16" and case.get("dist") == "int1000":
+        pytest.skip("integer case is fp32")
+    _check_exact(ddl, _w(dtype=dtype, **case))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("case", [SMALL[4], SMALL[7], SMALL[11], SMALL[16]])
+def test_fused_unaligned_buffers_match_oracle(ddl, case, dtype):
+    """Rank pointers that are not 16-byte aligned take the element-wise path."""
+    _check_exact(ddl, _w(dtype=dtype, **case), misalign=1)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("case", [SMALL[0], SMALL[1], SMALL[4], SMALL[7], SMALL[10], SMALL[12], SMALL[14]])
+def test_stepwise_matches_oracle(ddl, case, dtype):
+    if dtype == "f16" and case.get("dist") == "int1000":
+        pytest.skip("integer case is fp32")
+    _check_exact(ddl, _w(dtype=dtype, **case), mode="stepwise")
+
+
+@pytest.mark.parametrize("dtype,tol", [("f32", 1e-6), ("f16", 2e-3)])
+@pytest.mark.parametrize("case", [dict(P=16, N=100_003), dict(P=32, N=50_000, topo="torus", X=8, Y=4),
+                                  dict(P=64, N=30_001, topo="multiring", k=4, bucket_bytes=40_000)])
+def test_rankorder_within_tolerance(ddl, case, dtype, tol):
+    w = _w(dtype=dtype, **case)
+    host = _host_inputs(w)
+    bufs = device_bufs_from_host(host, DEV)
+    with ddl.Plan.for_workload(w, mode="rankorder") as plan:
+        plan.allreduce(bufs, w.scale)
+        torch.cuda.synchronize()
+    ref = oracle.ref64(host, w.scale, dtype)
+    got0 = to_numpy_bits(bufs[0])
+    got = oracle.f16_to_f32(got0).astype(np.float64) if dtype == "f16" else got0.astype(np.float64)
+    err = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert err <= tol, err
+    for r in range(1, w.P):
+        assert np.array_equal(to_numpy_bits(bufs[r]), got0)
+
+
+def test_device_generator_matches_host(ddl):
+    for dist, dtype, sigma in [("normal", "f32", 1e-3), ("normal", "f16", 1e-2), ("int1000", "f32", 1.0)]:
+        w = _w(P=3, N=100_003, dtype=dtype, dist=dist, sigma=sigma, seed=99)
+        dev = device_bufs_generated(w, DEV)
+        torch.cuda.synchronize()
+        for r in range(w.P):
+            assert np.array_equal(to_numpy_bits(dev[r]), w.rank_values(r)), (dist, dtype, r)
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads, in the configuration the bench times: every rank's
+# buffer compared on sampled elements (random and at every chunk edge) with
+# the oracle's closed form, and all ranks bitwise identical.
+# ---------------------------------------------------------------------------
+
+FULL = ["ring4_int", "torus4x4_resnet50", "torus8x4_resnet50_f16", "multiring64_resnet101", "ring16_lm300m",
+        "multiring16_lm300m", "torus4x4_lm300m"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload_sampled(ddl, name):
+    w = synth.WORKLOADS[name]
+    bufs = device_bufs_generated(w, DEV)
+    with ddl.Plan.for_workload(w) as plan:
+        plan.allreduce(bufs, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    for r in range(1, w.P):
+        assert torch.equal(bufs[r].view(torch.int16 if w.dtype == "f16" else torch.int32),
+                           bufs[0].view(torch.int16 if w.dtype == "f16" else torch.int32)), r
+    rng = np.random.default_rng(2017)
+    n_rand = w.N if w.N <= 65_536 else 60_000
+    idx = np.arange(w.N) if n_rand == w.N else np.unique(np.concatenate(
+        [rng.integers(0, w.N, n_rand), edge_samples(w)]))
+    x_rows = np.stack([w.rank_values(r, idx.astype(np.uint64)) for r in range(w.P)], axis=1)
+    want = oracle.closed_form(oracle_cfg(w), x_rows, idx.astype(np.uint64), w.scale)
+    got = to_numpy_bits(bufs[0][torch.from_numpy(idx).to(DEV)])
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"{bad.size} of {idx.size} sampled elements differ, e.g. idx {idx[bad[:5]]}"
+    if name == "ring4_int":
+        # integer inputs: the exact int64 total
+        ints = np.stack([w.rank_values(r) for r in range(w.P)]).astype(np.int64).sum(axis=0)
+        assert np.array_equal(to_numpy_bits(bufs[0]), ints.astype(np.float32))
+    del bufs
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# Bucket scheduler, host-buffer path, launches, argument checks on the GPU
+# ---------------------------------------------------------------------------
+
+def test_overlap_with_backward_matches_allreduce(ddl):
+    """Buckets signalled from a producer stream, reduced on the plan's side
+    stream, in reverse-layer order: same bits as the oracle."""
+    w = _w(P=8, N=400_000, layers=[50_000] * 8, bucket_bytes=300_000, seed=5)
+    host = _host_inputs(w)
+    ref = [h.copy() for h in host]
+    oracle.emulate(oracle_cfg(w), ref, w.scale)
+    bufs = [torch.zeros(w.N, dtype=torch.float32, device=DEV) for _ in range(w.P)]
+    src = device_bufs_from_host(host, DEV)
+    torch.cuda.synchronize()
+    main = torch.cuda.Stream()
+    with ddl.Plan.for_workload(w) as plan:
+        nb = plan.num_buckets
+        assert nb == 4
+        with torch.cuda.stream(main):
+            plan.overlap_begin(bufs, w.scale, stream=main)
+            for b in range(nb):                     # "back-propagation": output layers first
+                lo, hi = plan.bucket_range(b)
+                for r in range(w.P):
+                    bufs[r][lo:hi].copy_(src[r][lo:hi])
+                plan.bucket_ready(b, stream=main)
+            plan.overlap_end(stream=main)
+        main.synchronize()
+        torch.cuda.synchronize()
+        plan.check()
+        assert plan.launches == nb
+    for r in range(w.P):
+        assert np.array_equal(to_numpy_bits(bufs[r]), ref[r])
+
+
+def test_allreduce_host_buffers(ddl):
+    w = _w(P=6, N=50_001, topo="torus", X=3, Y=2, seed=8)
+    host = _host_inputs(w)
+    ref = [h.copy() for h in host]
+    oracle.emulate(oracle_cfg(w), ref, w.scale)
+    pinned = [torch.from_numpy(h.copy()).pin_memory() for h in host]
+    dev = [torch.empty(w.N, dtype=torch.float32, device=DEV) for _ in range(w.P)]
+    with ddl.Plan.for_workload(w) as plan:
+        plan.allreduce_host(pinned, dev, w.scale)
+        torch.cuda.synchronize()
+    for r in range(w.P):
+        assert np.array_equal(pinned[r].numpy(), ref[r])
+
+
+def test_launch_counts_and_checks(ddl):
+    w = _w(P=16, N=100_000, topo="torus", X=4, Y=4, bucket_bytes=100_000)
+    bufs = device_bufs_generated(w, DEV)
+    with ddl.Plan.for_workload(w) as plan:
+        nb = plan.num_buckets
+        plan.allreduce(bufs, w.scale)
+        assert plan.launches == nb
+        plan.set_mode("stepwise")
+        plan.allreduce(bufs, w.scale)
+        assert plan.launches == nb + nb * (2 * 3 + 2 * 3)
+        torch.cuda.synchronize()
+        plan.check()
+        # a host pointer is not device memory: refused before any launch
+        host = [np.zeros(w.N, dtype=np.float32) for _ in range(w.P)]
+        with pytest.raises(ddl.DDLError) as ei:
+            plan.allreduce([h.ctypes.data for h in host], w.scale)
+        assert ei.value.status == ddl.DDL_ERR_INVALID_ARG
+        # overlapping views of one tensor are refused
+        big = torch.zeros(w.N * w.P, device=DEV)
+        views = [big[i * (w.N - 1): i * (w.N - 1) + w.N] for i in range(w.P)]
+        with pytest.raises(ddl.DDLError):
+            plan.allreduce(views, w.scale)
