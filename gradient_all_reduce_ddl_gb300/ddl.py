@@ -35,7 +35,7 @@ EXPORTS = [
     "ddl_plan_create", "ddl_plan_set_layers", "ddl_plan_set_mode", "ddl_plan_set_kernel", "ddl_allreduce",
     "ddl_allreduce_bucket", "ddl_allreduce_host", "ddl_overlap_begin", "ddl_bucket_ready", "ddl_overlap_end",
     "ddl_plan_num_buckets", "ddl_plan_bucket_range", "ddl_plan_traffic", "ddl_plan_fold_order",
-    "ddl_plan_launches", "ddl_plan_check", "ddl_status_string", "ddl_plan_destroy",
+    "ddl_plan_launches", "ddl_plan_check", "ddl_status_string", "ddl_plan_destroy", "ddl_allreduce_noalloc",
 ]
 
 
@@ -72,6 +72,7 @@ _sig("ddl_plan_launches", _i, _vp, _P(_u64))
 _sig("ddl_plan_check", _i, _vp)
 _sig("ddl_status_string", ctypes.c_char_p, _i)
 _sig("ddl_plan_destroy", _i, _vp)
+_sig("ddl_allreduce_noalloc", _i, _i, _sz, _i, ddl_topology_t, _sz, _i, _P(_sz), _P(_vp), _f, _vp)
 
 
 class DDLError(RuntimeError):
@@ -197,6 +198,20 @@ def ddl_plan_check(plan):
 
 def ddl_plan_destroy(plan):
     _ok(_lib.ddl_plan_destroy(plan), "ddl_plan_destroy")
+
+
+def ddl_allreduce_noalloc(P, N, dtype, topology, bucket_bytes, layers, rank_bufs, scale, stream=None):
+    """Allocation-free all-reduce (no plan): tables in the library's static
+    device array.  dtype: DDL_FP32/DDL_FP16; topology: ddl_topology_t or dict;
+    layers: None or the tensor sizes in forward order."""
+    if isinstance(topology, dict):
+        topology = ddl_topology_t(topology.get("kind", DDL_RING), topology.get("k", 1), topology.get("X", 0),
+                                  topology.get("Y", 0))
+    layers = list(layers or [])
+    arr = (ctypes.c_size_t * max(1, len(layers)))(*[int(v) for v in layers])
+    _ok(_lib.ddl_allreduce_noalloc(P, N, dtype, topology, bucket_bytes, len(layers), arr,
+                                   _ptr_array(_dev_ptrs(rank_bufs)), scale, _stream_handle(stream)),
+        "ddl_allreduce_noalloc")
 
 
 # -- convenience object --------------------------------------------------------

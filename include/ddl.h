@@ -160,6 +160,33 @@ ddl_status_t ddl_overlap_begin(ddl_plan_t plan, void* const* rank_bufs, float sc
 ddl_status_t ddl_bucket_ready(ddl_plan_t plan, int bucket, void* stream);
 ddl_status_t ddl_overlap_end(ddl_plan_t plan, void* stream);
 
+/* Allocation-free form of ddl_allreduce, with no plan.  The web pages have no
+ * counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc -- a framework whose device memory all belongs to its own pool,
+ * a training loop that must not take cudaMalloc's implicit device
+ * synchronisation, or a deployment that fixes its memory footprint at
+ * start-up.  The arguments mean what they mean for ddl_plan_create,
+ * ddl_plan_set_layers (n_tensors = 0: no layer list) and ddl_allreduce; the
+ * mode is DDL_MODE_FUSED and the results are bit-identical to a plan's.
+ *  - The fused kernel's work tables live in one static 1 MiB device array
+ *    inside this library (every GPU that loads it holds the array until the
+ *    process exits) instead of plan-owned device memory.  Problems whose
+ *    tables need more than that (about 60,000 tiles of 8 KB per rank, i.e.
+ *    roughly 480 MB per rank) return DDL_ERR_UNSUPPORTED before any work.
+ *  - No cudaMalloc, cudaFree or other allocating call, and no host heap use.
+ *    The tables are copied from a static host buffer with cudaMemcpyAsync
+ *    from pageable memory, so the call waits for earlier work on `stream`.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the array, which keeps the last call's tables; each call
+ *    rewrites what it uses and clears the kernel error word.  Calls whose GPU
+ *    work overlaps (other streams, other host threads) race on the array and
+ *    must be ordered by the caller.  Host threads are serialised inside. */
+ddl_status_t ddl_allreduce_noalloc(int P, size_t N, ddl_dtype_t dtype, ddl_topology_t topo, size_t bucket_bytes,
+                                   int n_tensors, const size_t* numel_fwd_order, void* const* rank_bufs,
+                                   float scale, void* stream);
+
 /* Bucket table: *n buckets; bucket b covers elements [*begin, *end). */
 ddl_status_t ddl_plan_num_buckets(ddl_plan_t plan, int* n);
 ddl_status_t ddl_plan_bucket_range(ddl_plan_t plan, int bucket, size_t* begin, size_t* end);
