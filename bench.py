@@ -40,7 +40,9 @@ DEFAULT_WORKLOAD = "torus4x4_resnet50"
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the fused kernel,
 # from one ncu capture, keyed by (workload, kernel variant, sha256[:16] of the
 # kernel source it was taken on).  A changed kernel reports null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    ("torus4x4_resnet50", "ldg", "0e52a75d29912526"): 1_635_956_224 + 1_575_996_160,
+}
 
 KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]
 
