@@ -216,7 +216,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--mode", default="fused", choices=["fused", "stepwise", "rankorder"])
-    ap.add_argument("--kernel", default="auto", choices=["auto", "ldg", "bulk"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "ldg", "bulk", "bulkload"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -292,7 +292,7 @@ def main():
     launches_per_call = max(1, launches // args.steps)
     avg_call_ms = statistics.mean(per_call_ms)
     peak, peak_kind = measured_peak()
-    kernel_name = {"fused": "fold_ldg_kernel" if args.kernel != "bulk" else "fold_bulk_kernel",
+    kernel_name = {"fused": "fold_bulk_kernel" if args.kernel in ("bulk", "bulkload") else "fold_ldg_kernel",
                    "rankorder": "fold_ldg_kernel (rank order)", "stepwise": "step_kernel"}[args.mode]
     if args.mode == "stepwise":
         achieved = None

@@ -183,9 +183,15 @@ ddl_status_t run_bucket(ddl_plan* p, int b, void* const* bufs, bool aligned, flo
   fp.round_hops = (f16 && p->spec.mode == ddl::kFused) ? 1 : 0;
   fp.vector_ok = aligned ? 1 : 0;
   for (int r = 0; r < p->spec.P; ++r) fp.bufs[r] = bufs[r];
-  const int variant = p->kernel == DDL_KERNEL_BULK ? ddl::kVarBulk : ddl::kVarLdg;
+  // the staged pass needs 16-byte aligned buffers; otherwise the register
+  // pass runs (its element-wise path), with the same results
+  int variant = ddl::kVarLdg;
+  if (aligned && p->kernel == DDL_KERNEL_BULK) variant = ddl::kVarBulk;
+  if (aligned && p->kernel == DDL_KERNEL_BULK_LOAD) variant = ddl::kVarBulkLoad;
   const uint32_t n = bk.item_end - bk.item_begin;
   if (n == 0) return DDL_OK;
+  fp.n_items = n;
+  fp.tile_bytes = p->spec.tile_bytes;
   const cudaError_t e = ddl::launch_fold(fp, n, f16, variant, s);
   if (e != cudaSuccess) return cuda_status(e);
   ++p->launches;
@@ -265,9 +271,19 @@ ddl_status_t ddl_plan_set_mode(ddl_plan_t p, ddl_mode_t mode) {
 }
 
 ddl_status_t ddl_plan_set_kernel(ddl_plan_t p, ddl_kernel_t k) {
-  if (!p || k < DDL_KERNEL_AUTO || k > DDL_KERNEL_BULK) return DDL_ERR_INVALID_ARG;
+  if (!p || p->ov_active || k < DDL_KERNEL_AUTO || k > DDL_KERNEL_BULK_LOAD) return DDL_ERR_INVALID_ARG;
+  const bool staged = k == DDL_KERNEL_BULK || k == DDL_KERNEL_BULK_LOAD;
+  const uint32_t tile = staged ? ddl::bulk_tile_bytes(p->spec.P) : (uint32_t)ddl::kTileBytes;
   p->kernel = (int)k;
-  return DDL_OK;
+  if (tile == p->spec.tile_bytes) return DDL_OK;
+  const Spec old = p->spec;
+  p->spec.tile_bytes = tile;
+  const ddl_status_t st = rebuild(p);
+  if (st != DDL_OK) {
+    p->spec = old;
+    rebuild(p);
+  }
+  return st;
 }
 
 ddl_status_t ddl_allreduce(ddl_plan_t p, void* const* bufs, float scale, void* stream) {

@@ -251,6 +251,326 @@ __global__ void __launch_bounds__(kThreads, 2) fold_ldg_kernel(const __grid_cons
   }
 }
 
+// ---------------------------------------------------------------------------
+// Variants 2 and 3: shared-memory staged pass with bulk asynchronous copies,
+// warp-specialised.
+//
+// Persistent CTAs (one per SM) of 1 producer warp + 8 consumer warps walk
+// their work items through a ring of kStages stages in shared memory.  The
+// producer waits until the consumers have released a stage (its "empty"
+// mbarrier), publishes the next item's bounds and fold order, arms the
+// stage's "full" mbarrier with the byte count, and issues one cp.async.bulk
+// per rank (global -> shared).  Consumers wait on "full", fold their columns
+// from shared memory in the schedule's order, and release the stage.  The
+// result goes back either from registers (one 16-byte store per rank, variant
+// 3) or as one shared tile that an elected consumer writes to every rank with
+// cp.async.bulk (shared -> global, variant 2).  The producer never joins a
+// consumer barrier, so its table reads stay off the consumers' path.  Every
+// wait is bounded: a wait that runs out sets kErrWaitTimeout and the warp
+// leaves its loop; the CTA then drains its own copies (bounded) and returns.
+// ---------------------------------------------------------------------------
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kBulkThreads = kConsumers + 32;
+constexpr int kStages = 3;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
+
+struct BulkMeta {
+  uint64_t eb, ee;   // item elements [eb, ee)
+  uint64_t vb, ve;   // 16-byte columns [vb, ve) staged through shared memory
+  uint32_t inner, groups;
+  uint32_t ok, order_off;
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < (1u << 28); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u && global_ns() - t0 > kWaitNs) break;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src_smem)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// barrier 1 among the consumer warps only (the producer never joins it)
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+// the same barrier, returning whether any consumer passed `flag` (so a
+// timeout is seen by all consumers at once and they leave together)
+__device__ __forceinline__ bool consumer_sync_or(bool flag) {
+  uint32_t any;
+  asm volatile(
+      "{\n\t.reg .pred f, a;\n\t"
+      "setp.ne.u32 f, %1, 0;\n\t"
+      "bar.red.or.pred a, 1, %2, f;\n\t"
+      "selp.u32 %0, 1, 0, a;\n\t}"
+      : "=r"(any)
+      : "r"((uint32_t)flag), "n"(kConsumers)
+      : "memory");
+  return any != 0;
+}
+
+// shared memory: stages x P x tile | 2 x tile output | stages x kMaxP order | meta | barriers
+__host__ __device__ constexpr uint32_t bulk_smem_bytes(uint32_t P, uint32_t tile) {
+  return (uint32_t)kStages * P * tile + 2u * tile + (uint32_t)kStages * kMaxP +
+         (uint32_t)(kStages * sizeof(BulkMeta)) + (uint32_t)(2 * kStages * sizeof(uint64_t)) + 16u;
+}
+
+template <bool F16>
+__device__ void fold_scalar_ordered(const FoldParams& p, const uint8_t* order, uint64_t e, int inner, int groups,
+                                    bool rh) {
+  float in = 0.f, out = 0.f;
+  int h = 0, g = 0;
+  for (int t = 0; t < p.P; ++t) {
+    const float v = load_elem<F16>(static_cast<const char*>(p.bufs[order[t]]), e);
+    const Ctl c = ctl_at(t, h, g, inner, groups, p.P, rh);
+    fold_lanes<1>(&in, &out, &v, c);
+    if (++h == inner) {
+      h = 0;
+      ++g;
+    }
+  }
+  const float r = __fmul_rn(out, p.scale);
+  for (int t = 0; t < p.P; ++t) store_elem<F16>(static_cast<char*>(p.bufs[order[t]]), e, r);
+}
+
+template <bool F16, bool kBulkStore>
+__global__ void __launch_bounds__(kBulkThreads, 1) fold_bulk_kernel(const __grid_constant__ FoldParams p) {
+  constexpr int L = F16 ? 8 : 4;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const uint32_t P = (uint32_t)p.P, T = p.tile_bytes;
+  unsigned char* stage = smem;
+  unsigned char* outb = smem + (uint32_t)kStages * P * T;
+  uint8_t* s_order = outb + 2u * T;
+  BulkMeta* s_meta = reinterpret_cast<BulkMeta*>(s_order + kStages * kMaxP);
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_meta + kStages);
+  uint64_t* empty = full + kStages;
+
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
+  const uint32_t my_n = p.n_items > blockIdx.x ? (p.n_items - 1u - blockIdx.x) / gridDim.x + 1u : 0u;
+  const bool rh = F16 && p.round_hops;
+
+  if (tid == 0) {
+    for (int k = 0; k < kStages; ++k) {
+      mbar_init(&full[k], 1);
+      mbar_init(&empty[k], kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  uint32_t issued = 0, consumed = 0;  // items this thread's role got through
+  bool timed_out = false;
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer warp ----------------
+    for (uint32_t s = 0; s < my_n; ++s) {
+      const uint32_t k = s % kStages;
+      if (s >= (uint32_t)kStages && !mbar_wait(&empty[k], ((s / kStages) - 1u) & 1u)) {
+        timed_out = true;
+        break;
+      }
+      if (lane == 0) {
+        const Item item = p.items[p.item0 + blockIdx.x + s * gridDim.x];
+        BulkMeta m;
+        m.eb = item.begin;
+        m.ee = item.begin + item.len;
+        m.vb = (m.eb + L - 1) / L;
+        m.ve = m.ee / L;
+        if (m.ve < m.vb) m.ve = m.vb;
+        m.ok = item.seg < p.n_segs;
+        m.inner = m.groups = 1;
+        m.order_off = 0;
+        if (m.ok) {
+          const Segment sg = p.segs[item.seg];
+          m.ok = (uint32_t)sg.inner * sg.groups == P && sg.order_off + P <= p.n_orders;
+          m.inner = sg.inner;
+          m.groups = sg.groups;
+          m.order_off = sg.order_off;
+        }
+        if (!m.ok) atomicOr(p.err, kErrBadOrder);
+        s_meta[k] = m;
+      }
+      __syncwarp();
+      const BulkMeta m = s_meta[k];
+      if (m.ok)
+        for (uint32_t t = lane; t < P; t += 32) {
+          const uint32_t r = p.orders[m.order_off + t];
+          s_order[k * kMaxP + t] = (uint8_t)(r < P ? r : 0);
+        }
+      const uint32_t bytes = m.ok ? (uint32_t)(m.ve - m.vb) * 16u : 0u;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&full[k], bytes * P);  // release: meta and order are published
+      __syncwarp();
+      if (bytes)
+        for (uint32_t r = lane; r < P; r += 32)
+          bulk_load(stage + ((size_t)k * P + r) * T, static_cast<const char*>(p.bufs[r]) + m.vb * 16u, bytes,
+                    &full[k]);
+      issued = s + 1;
+    }
+    if (timed_out && lane == 0) atomicOr(p.err, kErrWaitTimeout);
+  } else {
+    // ---------------- consumer warps ----------------
+    for (uint32_t s = 0; s < my_n; ++s) {
+      const uint32_t k = s % kStages, j = s & 1u;
+      const bool ok = mbar_wait(&full[k], (s / kStages) & 1u);
+      if constexpr (kBulkStore) {
+        if (tid == 0) bulk_wait_read_1();  // output tile j was read by item s-2's stores
+        if (consumer_sync_or(!ok)) {       // uniform: the named barrier below needs every consumer
+          timed_out = true;
+          break;
+        }
+      } else if (!ok) {
+        timed_out = true;
+        break;
+      }
+      const BulkMeta m = s_meta[k];
+      const uint8_t* ord = s_order + k * kMaxP;
+      const uint32_t ncols = (uint32_t)(m.ve - m.vb);
+      if (m.ok) {
+        const unsigned char* st = stage + (size_t)k * P * T;
+        for (uint32_t c = tid; c < ncols; c += kConsumers) {
+          float in[L], out[L];
+          int h = 0, g = 0;
+          for (uint32_t t0 = 0; t0 < P; t0 += 8) {
+            uint4 raw[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (t0 + q < P) raw[q] = *reinterpret_cast<const uint4*>(st + (size_t)ord[t0 + q] * T + c * 16u);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (t0 + q < P) {
+                float f[L];
+                unpack<F16>(raw[q], f);
+                const Ctl ctl = ctl_at((int)(t0 + q), h, g, (int)m.inner, (int)m.groups, (int)P, rh);
+                fold_lanes<L>(in, out, f, ctl);
+                if (++h == (int)m.inner) {
+                  h = 0;
+                  ++g;
+                }
+              }
+            }
+          }
+          float r[L];
+#pragma unroll
+          for (int l = 0; l < L; ++l) r[l] = __fmul_rn(out[l], p.scale);
+          const uint4 res = pack<F16>(r);
+          if constexpr (kBulkStore) {
+            *reinterpret_cast<uint4*>(outb + (size_t)j * T + c * 16u) = res;
+          } else {
+            for (uint32_t t = 0; t < P; ++t) __stcs(reinterpret_cast<uint4*>(p.bufs[t]) + m.vb + c, res);
+          }
+        }
+        // elements of a column cut by the item's ends: straight from global
+        const uint64_t nh = (m.ve > m.vb) ? m.vb * L - m.eb : m.ee - m.eb;
+        const uint64_t nt = (m.ve > m.vb) ? m.ee - m.ve * L : 0;
+        if (tid < nh + nt) {
+          const uint64_t e = tid < nh ? m.eb + tid : m.ve * L + (tid - nh);
+          fold_scalar_ordered<F16>(p, ord, e, (int)m.inner, (int)m.groups, rh);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[k]);  // this warp is done with stage k
+      if constexpr (kBulkStore) {
+        fence_async_smem();
+        consumer_sync();
+        if (tid == 0) {
+          if (m.ok && ncols)
+            for (uint32_t r = 0; r < P; ++r)
+              bulk_store(static_cast<char*>(p.bufs[r]) + m.vb * 16u, outb + (size_t)j * T, ncols * 16u);
+          bulk_commit();  // one group per item, so "all but the newest" means item s-1
+        }
+      }
+      consumed = s + 1;
+    }
+    if (timed_out && lane == 0) atomicOr(p.err, kErrWaitTimeout);
+  }
+
+  // Both roles leave their loops (every wait is bounded).  Publish how far the
+  // producer got, then let loads that nobody consumed land before exit.
+  __shared__ uint32_t s_issued, s_consumed;
+  if (warp == kConsumerWarps && lane == 0) s_issued = issued;
+  if (tid == 0) s_consumed = consumed;
+  __syncthreads();
+  if (tid == 0) {
+    for (uint32_t q = s_consumed; q < s_issued; ++q) mbar_wait(&full[q % kStages], (q / kStages) & 1u);
+    bulk_wait_all();
+  }
+}
+
+template <bool F16, bool kBulkStore>
+cudaError_t launch_bulk(const FoldParams& p, uint32_t n_items, cudaStream_t stream) {
+  const uint32_t smem = bulk_smem_bytes((uint32_t)p.P, p.tile_bytes);
+  int dev = 0, sms = 0, max_smem = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if (smem > (uint32_t)max_smem || p.tile_bytes % 16 != 0 || p.tile_bytes == 0) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(fold_bulk_kernel<F16, kBulkStore>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  const uint32_t grid = n_items < (uint32_t)sms ? n_items : (uint32_t)sms;
+  fold_bulk_kernel<F16, kBulkStore><<<grid, kBulkThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <bool F16>
 cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t stream) {
   fold_ldg_kernel<F16, 2, 8><<<n_items, kThreads, 0, stream>>>(p);
@@ -261,7 +581,10 @@ cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t strea
 
 cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream) {
   if (n_items == 0) return cudaSuccess;
-  (void)variant;
+  if (variant == kVarBulk)
+    return f16 ? launch_bulk<true, true>(p, n_items, stream) : launch_bulk<false, true>(p, n_items, stream);
+  if (variant == kVarBulkLoad)
+    return f16 ? launch_bulk<true, false>(p, n_items, stream) : launch_bulk<false, false>(p, n_items, stream);
   return f16 ? launch_ldg<true>(p, n_items, stream) : launch_ldg<false>(p, n_items, stream);
 }
 

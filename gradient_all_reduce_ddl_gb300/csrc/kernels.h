@@ -29,7 +29,9 @@ struct FoldParams {
   float scale;
   int32_t round_hops;  // binary16 storage: round every intermediate result
   int32_t vector_ok;   // every rank pointer is 16-byte aligned
-  int32_t pad;
+  uint32_t n_items;    // items in this launch (persistent kernels)
+  uint32_t tile_bytes; // bytes per rank of the largest item
+  uint32_t pad;
   void* bufs[kMaxP];   // rank r's buffer
 };
 
@@ -44,7 +46,7 @@ struct StepParams {
 };
 
 // Variants of the fused pass.
-enum FoldVariant : int { kVarLdg = 1, kVarBulk = 2 };
+enum FoldVariant : int { kVarLdg = 1, kVarBulk = 2, kVarBulkLoad = 3 };
 
 cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, uint32_t n_xfers, uint64_t max_len, bool f16, cudaStream_t stream);

@@ -92,7 +92,7 @@ struct Builder {
     for (int r : order) t->orders.push_back((uint8_t)r);
     const uint32_t seg = (uint32_t)t->segs.size();
     t->segs.push_back(g);
-    const uint64_t tile = (uint64_t)kTileBytes / (uint64_t)s.esize;
+    const uint64_t tile = (uint64_t)s.tile_bytes / (uint64_t)s.esize;
     for (uint64_t a = lo, end = lo + len; a < end;) {
       const uint64_t next = std::min(end, (a / tile + 1) * tile);
       t->items.push_back(Item{a, (uint32_t)(next - a), seg});
@@ -228,6 +228,12 @@ struct Builder {
 };
 
 }  // namespace
+
+uint32_t bulk_tile_bytes(int P) {
+  uint32_t t = 16384;
+  while (t > 256 && (uint64_t)t * (uint64_t)P > 65536) t >>= 1;
+  return t;
+}
 
 bool ring_multipliers(int P, int k, std::vector<int>* out) {
   out->clear();

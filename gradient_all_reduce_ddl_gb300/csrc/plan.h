@@ -69,7 +69,12 @@ struct Spec {
   uint64_t bucket_bytes = 0;
   std::vector<uint64_t> layers;
   int mode = kFused;
+  uint32_t tile_bytes = kTileBytes;  // bytes per rank in one work item
 };
+
+// Work-item size of the shared-memory-staged pass: P ranks' tiles of one
+// pipeline stage fill about 64 KB, between 256 B and 16 KB per rank.
+uint32_t bulk_tile_bytes(int P);
 
 struct Tables {
   std::vector<Bucket> buckets;

@@ -29,7 +29,7 @@ DDL_RING, DDL_MULTIRING, DDL_TORUS = 0, 1, 2
 # ddl_mode_t
 DDL_MODE_FUSED, DDL_MODE_STEPWISE, DDL_MODE_RANKORDER = 0, 1, 2
 # ddl_kernel_t
-DDL_KERNEL_AUTO, DDL_KERNEL_LDG, DDL_KERNEL_BULK = 0, 1, 2
+DDL_KERNEL_AUTO, DDL_KERNEL_LDG, DDL_KERNEL_BULK, DDL_KERNEL_BULK_LOAD = 0, 1, 2, 3
 
 EXPORTS = [
     "ddl_plan_create", "ddl_plan_set_layers", "ddl_plan_set_mode", "ddl_plan_set_kernel", "ddl_allreduce",
@@ -219,7 +219,7 @@ def ddl_allreduce_noalloc(P, N, dtype, topology, bucket_bytes, layers, rank_bufs
 TOPOLOGIES = {"ring": DDL_RING, "multiring": DDL_MULTIRING, "torus": DDL_TORUS}
 DTYPES = {"f32": DDL_FP32, "f16": DDL_FP16}
 MODES = {"fused": DDL_MODE_FUSED, "stepwise": DDL_MODE_STEPWISE, "rankorder": DDL_MODE_RANKORDER}
-KERNELS = {"auto": DDL_KERNEL_AUTO, "ldg": DDL_KERNEL_LDG, "bulk": DDL_KERNEL_BULK}
+KERNELS = {"auto": DDL_KERNEL_AUTO, "ldg": DDL_KERNEL_LDG, "bulk": DDL_KERNEL_BULK, "bulkload": DDL_KERNEL_BULK_LOAD}
 
 
 class Plan:

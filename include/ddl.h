@@ -90,7 +90,9 @@ typedef enum {
 typedef enum {
   DDL_KERNEL_AUTO = 0,  /* the library's choice */
   DDL_KERNEL_LDG = 1,   /* fused pass with 16-byte register loads and stores */
-  DDL_KERNEL_BULK = 2   /* fused pass staged through shared memory by bulk async copies */
+  DDL_KERNEL_BULK = 2,  /* fused pass staged through shared memory by bulk async copies,
+                           loads and stores */
+  DDL_KERNEL_BULK_LOAD = 3  /* bulk async loads into shared memory, stores from registers */
 } ddl_kernel_t;
 
 typedef struct ddl_plan* ddl_plan_t;

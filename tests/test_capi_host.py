@@ -96,6 +96,19 @@ def test_workload_tables_match_oracle(ddl, name):
             assert plan.fold_order(i) == (o_ord.tolist(), o_in, o_gr)
 
 
+@pytest.mark.parametrize("case", [CASES[2], CASES[5], CASES[7], CASES[9]])
+def test_staged_kernel_tables_match_oracle(ddl, case):
+    """Selecting the staged kernel rebuilds the work items at its tile size;
+    the fold orders stay the oracle's."""
+    plan, cfg = _pair(**case)
+    with plan:
+        plan.set_kernel("bulk")
+        assert plan.buckets() == oracle.buckets(cfg)
+        for i in range(cfg.N):
+            o_ord, o_in, o_gr = oracle.fold_order(cfg, i)
+            assert plan.fold_order(i) == (o_ord.tolist(), o_in, o_gr), i
+
+
 def test_rankorder_and_stepwise_tables(ddl):
     plan, cfg = _pair(P=5, N=50, topo="torus", X=5, Y=1, mode="rankorder")
     with plan:

@@ -92,19 +92,21 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("kernel", ["ldg", "bulk", "bulkload"])
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
-def test_fused_matches_oracle(ddl, case, dtype):
+def test_fused_matches_oracle(ddl, case, dtype, kernel):
     if dtype == "f16" and case.get("dist") == "int1000":
         pytest.skip("integer case is fp32")
-    _check_exact(ddl, _w(dtype=dtype, **case))
+    _check_exact(ddl, _w(dtype=dtype, **case), kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", ["ldg", "bulk"])
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
 @pytest.mark.parametrize("case", [SMALL[4], SMALL[7], SMALL[11], SMALL[16]])
-def test_fused_unaligned_buffers_match_oracle(ddl, case, dtype):
+def test_fused_unaligned_buffers_match_oracle(ddl, case, dtype, kernel):
     """Rank pointers that are not 16-byte aligned take the element-wise path."""
-    _check_exact(ddl, _w(dtype=dtype, **case), misalign=1)
+    _check_exact(ddl, _w(dtype=dtype, **case), misalign=1, kernel=kernel)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
@@ -153,11 +155,12 @@ FULL = ["ring4_int", "torus4x4_resnet50", "torus8x4_resnet50_f16", "multiring64_
         "multiring16_lm300m", "torus4x4_lm300m"]
 
 
+@pytest.mark.parametrize("kernel", ["auto", "bulk", "bulkload"])
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_workload_sampled(ddl, name):
+def test_full_size_workload_sampled(ddl, name, kernel):
     w = synth.WORKLOADS[name]
     bufs = device_bufs_generated(w, DEV)
-    with ddl.Plan.for_workload(w) as plan:
+    with ddl.Plan.for_workload(w, kernel=kernel) as plan:
         plan.allreduce(bufs, w.scale)
         torch.cuda.synchronize()
         plan.check()
