@@ -221,6 +221,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one ddl_allreduce in a CUDA graph and replay it each step")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = synth.WORKLOADS[args.workload]
@@ -258,6 +260,20 @@ def main():
     torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(smi_gpu_id(local if ws > 1 else 0))
+    graph = None
+    if args.graph:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        l0 = plan.launches
+        with torch.cuda.graph(graph, stream=cap):
+            plan.allreduce(bufs, w.scale, cap)
+        graph_launches = plan.launches - l0
+        stream.wait_stream(cap)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+
     clocks.start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     launches0 = plan.launches
@@ -269,14 +285,17 @@ def main():
     start.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
-        plan.allreduce(bufs, w.scale, stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            plan.allreduce(bufs, w.scale, stream)
         ev[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     clocks.mark("t1")
     clk = clocks.stop()
-    launches = plan.launches - launches0
+    launches = plan.launches - launches0 if graph is None else graph_launches * args.steps
     total_ms = start.elapsed_time(end)
     per_call_ms = [a.elapsed_time(b) for a, b in ev]
     t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -343,6 +362,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
                 "config": {"workload": w.name, "P": w.P, "N": w.N, "schedule": schedule_name(w), "mode": args.mode,
                            "kernel": args.kernel, "buckets": nb, "bytes_per_step": nbytes,
+                           "launch": "CUDA graph replay" if args.graph else "ddl_allreduce call per step",
                            "elems_per_s": round(elems, 1), "frac_of_hbm": round(gbs / ws / peak, 4),
                            "l2": f"inputs {w.P * w.N * w.esize / 1e9:.2f} GB per replica, larger than the 129 MB L2",
                            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU, P logical ranks"},

@@ -171,10 +171,22 @@ __device__ __forceinline__ bool load_item(const FoldParams& p, char** s_ptr, Ite
 }
 
 // ---------------------------------------------------------------------------
-// Variant 1: register pass.  V columns per thread, B ranks' loads in flight.
+// Variant 1: register pass.  V columns per thread, B ranks' loads in flight,
+// sized for MINB CTAs per SM.  V * kThreads columns cover the largest item.
 // ---------------------------------------------------------------------------
-template <bool F16, int V, int B>
-__global__ void __launch_bounds__(kThreads, 2) fold_ldg_kernel(const __grid_constant__ FoldParams p) {
+#ifndef DDL_LDG_F32_B
+#define DDL_LDG_F32_B 8
+#endif
+#ifndef DDL_LDG_F16_B
+#define DDL_LDG_F16_B 8
+#endif
+#ifndef DDL_LDG_MINB
+#define DDL_LDG_MINB 2
+#endif
+
+template <bool F16, int V, int B, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) fold_ldg_kernel(const __grid_constant__ FoldParams p) {
+  static_assert(V * kThreads * 16 >= kTileBytes, "an item must fit one pass of the columns");
   constexpr int L = F16 ? 8 : 4;  // elements per 16-byte column
   __shared__ char* s_ptr[kMaxP];
   __shared__ Item s_item;
@@ -573,7 +585,11 @@ cudaError_t launch_bulk(const FoldParams& p, uint32_t n_items, cudaStream_t stre
 
 template <bool F16>
 cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t stream) {
-  fold_ldg_kernel<F16, 2, 8><<<n_items, kThreads, 0, stream>>>(p);
+  if constexpr (F16) {
+    fold_ldg_kernel<true, 2, DDL_LDG_F16_B, DDL_LDG_MINB><<<n_items, kThreads, 0, stream>>>(p);
+  } else {
+    fold_ldg_kernel<false, 2, DDL_LDG_F32_B, DDL_LDG_MINB><<<n_items, kThreads, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

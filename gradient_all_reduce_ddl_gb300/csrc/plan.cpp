@@ -229,6 +229,12 @@ struct Builder {
 
 }  // namespace
 
+uint32_t ldg_tile_bytes(uint64_t bytes_per_rank) {
+  uint32_t t = kTileBytes;
+  while (t > 1024 && bytes_per_rank < (uint64_t)t * 304) t >>= 1;
+  return t;
+}
+
 uint32_t bulk_tile_bytes(int P) {
   uint32_t t = 16384;
   while (t > 256 && (uint64_t)t * (uint64_t)P > 65536) t >>= 1;

@@ -76,6 +76,11 @@ struct Spec {
 // pipeline stage fill about 64 KB, between 256 B and 16 KB per rank.
 uint32_t bulk_tile_bytes(int P);
 
+// Work-item size of the register pass: kTileBytes, or smaller (down to 1 KB)
+// when a rank's buffer is too small to give every SM of a large GPU
+// (2 x 152 items) work at that size.
+uint32_t ldg_tile_bytes(uint64_t bytes_per_rank);
+
 struct Tables {
   std::vector<Bucket> buckets;
   std::vector<Segment> segs;

@@ -12,7 +12,9 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libddl.so")
+# DDL_LIBRARY may name another build of the same library (e.g. one compiled
+# with different kernel tuning macros); the default is the in-tree build.
+LIB_PATH = os.environ.get("DDL_LIBRARY") or os.path.join(_HERE, "libddl.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is not built; run gradient_all_reduce_ddl_gb300.build.build() "
