@@ -40,6 +40,9 @@ struct ddl_plan {
   // last rank-pointer set that passed the device-pointer check
   std::vector<void*> checked;
   bool checked_aligned = false;
+  // host-buffer pipeline: copy-in, compute and copy-out streams, events
+  cudaStream_t hs[3] = {nullptr, nullptr, nullptr};
+  std::vector<cudaEvent_t> hev;
 };
 
 namespace {
@@ -199,6 +202,44 @@ ddl_status_t run_bucket(ddl_plan* p, int b, void* const* bufs, bool aligned, flo
   return DDL_OK;
 }
 
+// Fused pass over items [ia, ib) of bucket b only (an element range of it).
+ddl_status_t run_items(ddl_plan* p, uint32_t ia, uint32_t ib, void* const* bufs, bool aligned, float scale,
+                       cudaStream_t s) {
+  if (ib <= ia) return DDL_OK;
+  const bool f16 = p->spec.esize == 2;
+  ddl::FoldParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.items = p->d_items;
+  fp.segs = p->d_segs;
+  fp.orders = p->d_orders;
+  fp.err = p->d_err;
+  fp.item0 = ia;
+  fp.n_segs = (uint32_t)p->tab.segs.size();
+  fp.n_orders = (uint32_t)p->tab.orders.size();
+  fp.P = p->spec.P;
+  fp.scale = scale;
+  fp.round_hops = (f16 && p->spec.mode == ddl::kFused) ? 1 : 0;
+  fp.vector_ok = aligned ? 1 : 0;
+  for (int r = 0; r < p->spec.P; ++r) fp.bufs[r] = bufs[r];
+  int variant = ddl::kVarLdg;
+  if (aligned && p->kernel == DDL_KERNEL_BULK) variant = ddl::kVarBulk;
+  if (aligned && p->kernel == DDL_KERNEL_BULK_LOAD) variant = ddl::kVarBulkLoad;
+  fp.n_items = ib - ia;
+  fp.tile_bytes = p->spec.tile_bytes;
+  const cudaError_t e = ddl::launch_fold(fp, ib - ia, f16, variant, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  ++p->launches;
+  return DDL_OK;
+}
+
+// First item of bucket b that starts at or after element x.
+uint32_t item_at(const ddl_plan* p, const ddl::Bucket& bk, uint64_t x) {
+  auto first = p->tab.items.begin() + bk.item_begin, last = p->tab.items.begin() + bk.item_end;
+  return (uint32_t)(std::lower_bound(first, last, x,
+                                     [](const ddl::Item& it, uint64_t v) { return it.begin < v; }) -
+                    p->tab.items.begin());
+}
+
 ddl_status_t prepare(ddl_plan* p, void* const* bufs, bool* aligned) {
   if (!p || !bufs) return DDL_ERR_INVALID_ARG;
   // repeated call with the pointer set that passed every check last time
@@ -319,30 +360,121 @@ ddl_status_t ddl_allreduce_bucket(ddl_plan_t p, int bucket, void* const* bufs, f
   return run_bucket(p, bucket, bufs, aligned, scale, static_cast<cudaStream_t>(stream));
 }
 
+// Zero-copy form: the fused pass works on host buffers that the GPU can
+// reach directly (page-locked, managed, or pageable where the system gives
+// the GPU coherent access to it).
+static ddl_status_t allreduce_in_host_memory(ddl_plan* p, void* const* host_bufs, float scale, cudaStream_t s) {
+  bool al = false;
+  ddl_status_t st = check_bufs(p, host_bufs, false, &al);
+  if (st != DDL_OK) return st;
+  st = ensure_device(p);
+  if (st != DDL_OK) return st;
+  int pageable = 0;
+  cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, p->device);
+  for (int r = 0; r < p->spec.P; ++r) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, host_bufs[r]) != cudaSuccess) {
+      cudaGetLastError();
+      return DDL_ERR_INVALID_ARG;
+    }
+    const bool reach = at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeManaged ||
+                       (at.type == cudaMemoryTypeUnregistered && pageable);
+    if (!reach) return DDL_ERR_INVALID_ARG;
+  }
+  if (p->spec.mode == ddl::kStepwise) return DDL_ERR_UNSUPPORTED;
+  for (int b = 0; b < (int)p->tab.buckets.size(); ++b) {
+    st = run_bucket(p, b, host_bufs, al, scale, s);
+    if (st != DDL_OK) return st;
+  }
+  return DDL_OK;
+}
+
 ddl_status_t ddl_allreduce_host(ddl_plan_t p, void* const* host_bufs, void* const* dev_bufs, float scale,
                                 void* stream) {
   if (!p || !host_bufs) return DDL_ERR_INVALID_ARG;
   for (int r = 0; r < p->spec.P; ++r)
     if (!host_bufs[r]) return DDL_ERR_INVALID_ARG;
+  if (p->ov_active) return DDL_ERR_INVALID_ARG;
+  if (!dev_bufs) return allreduce_in_host_memory(p, host_bufs, scale, static_cast<cudaStream_t>(stream));
   bool aligned = false;
   ddl_status_t st = prepare(p, dev_bufs, &aligned);
   if (st != DDL_OK) return st;
   if (p->ov_active) return DDL_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t bytes = p->spec.N * (size_t)p->spec.esize;
-  for (int r = 0; r < p->spec.P; ++r) {
-    const cudaError_t e = cudaMemcpyAsync(dev_bufs[r], host_bufs[r], bytes, cudaMemcpyHostToDevice, s);
+  const size_t es = (size_t)p->spec.esize;
+  const int P = p->spec.P;
+  auto copy_all = [&](uint64_t lo, uint64_t hi, cudaMemcpyKind kind, cudaStream_t cs) -> cudaError_t {
+    for (int r = 0; r < P; ++r) {
+      char* h = static_cast<char*>(host_bufs[r]) + lo * es;
+      char* d = static_cast<char*>(dev_bufs[r]) + lo * es;
+      const cudaError_t e = kind == cudaMemcpyHostToDevice ? cudaMemcpyAsync(d, h, (hi - lo) * es, kind, cs)
+                                                           : cudaMemcpyAsync(h, d, (hi - lo) * es, kind, cs);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  };
+  if (p->spec.mode == ddl::kStepwise) {
+    // whole buckets move through the steps: copy in, reduce, copy out
+    cudaError_t e = copy_all(0, p->spec.N, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_status(e);
+    for (int b = 0; b < (int)p->tab.buckets.size(); ++b) {
+      st = run_bucket(p, b, dev_bufs, aligned, scale, s);
+      if (st != DDL_OK) return st;
+    }
+    e = copy_all(0, p->spec.N, cudaMemcpyDeviceToHost, s);
+    return cuda_status(e);
   }
+  // Every output element depends only on the same element of every rank, so
+  // the copy-in, the fused pass and the copy-out pipeline over element ranges
+  // (tile-aligned, so each range is a run of whole work items) on three
+  // streams: copy-in of range i+1 and copy-out of range i-1 overlap the pass
+  // over range i, and the two copy directions overlap each other.
+  constexpr int kMaxRanges = 32;
+  const uint64_t tile = (uint64_t)p->spec.tile_bytes / es;
+  uint64_t R = (p->spec.N + kMaxRanges - 1) / kMaxRanges;
+  R = ((R + tile - 1) / tile) * tile;
+  const uint64_t min_r = ((uint64_t)(1u << 20) / es + tile - 1) / tile * tile;  // >= 1 MiB per rank
+  if (R < min_r) R = min_r;
+  cudaError_t e = cudaSuccess;
+  if (!p->hs[0])
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&p->hs[i], cudaStreamNonBlocking);
+  const size_t need = 1 + 3 * (size_t)(kMaxRanges + p->tab.buckets.size());
+  while (e == cudaSuccess && p->hev.size() < need) {
+    cudaEvent_t ev;
+    e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) p->hev.push_back(ev);
+  }
+  if (e != cudaSuccess) return cuda_status(e);
+  cudaStream_t sin = p->hs[0], scomp = p->hs[1], sout = p->hs[2];
+  size_t evi = 0;
+  cudaEvent_t start = p->hev[evi++];
+  e = cudaEventRecord(start, s);
+  for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(p->hs[i], start, 0);
+  if (e != cudaSuccess) return cuda_status(e);
+  // buckets run from the highest addresses down; ranges ascend inside each
   for (int b = 0; b < (int)p->tab.buckets.size(); ++b) {
-    st = run_bucket(p, b, dev_bufs, aligned, scale, s);
-    if (st != DDL_OK) return st;
+    const ddl::Bucket& bk = p->tab.buckets[b];
+    for (uint64_t lo = bk.lo; lo < bk.hi;) {
+      uint64_t hi = (lo / R + 1) * R;
+      if (hi > bk.hi) hi = bk.hi;
+      cudaEvent_t ein = p->hev[evi++], ecomp = p->hev[evi++];
+      e = copy_all(lo, hi, cudaMemcpyHostToDevice, sin);
+      if (e == cudaSuccess) e = cudaEventRecord(ein, sin);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(scomp, ein, 0);
+      if (e != cudaSuccess) return cuda_status(e);
+      st = run_items(p, item_at(p, bk, lo), item_at(p, bk, hi), dev_bufs, aligned, scale, scomp);
+      if (st != DDL_OK) return st;
+      e = cudaEventRecord(ecomp, scomp);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(sout, ecomp, 0);
+      if (e == cudaSuccess) e = copy_all(lo, hi, cudaMemcpyDeviceToHost, sout);
+      if (e != cudaSuccess) return cuda_status(e);
+      lo = hi;
+    }
   }
-  for (int r = 0; r < p->spec.P; ++r) {
-    const cudaError_t e = cudaMemcpyAsync(host_bufs[r], dev_bufs[r], bytes, cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) return cuda_status(e);
-  }
-  return DDL_OK;
+  cudaEvent_t done = p->hev[evi++];
+  e = cudaEventRecord(done, sout);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, done, 0);
+  return cuda_status(e);
 }
 
 ddl_status_t ddl_overlap_begin(ddl_plan_t p, void* const* bufs, float scale, void* stream) {
@@ -445,6 +577,12 @@ ddl_status_t ddl_plan_destroy(ddl_plan_t p) {
     if (p->side) cudaStreamSynchronize(p->side);
     free_device_tables(p);
     cudaFree(p->d_err);
+    for (int i = 0; i < 3; ++i)
+      if (p->hs[i]) {
+        cudaStreamSynchronize(p->hs[i]);
+        cudaStreamDestroy(p->hs[i]);
+      }
+    for (cudaEvent_t ev : p->hev) cudaEventDestroy(ev);
     for (cudaEvent_t ev : p->ev_ready) cudaEventDestroy(ev);
     if (p->ev_done) cudaEventDestroy(p->ev_done);
     if (p->side) cudaStreamDestroy(p->side);

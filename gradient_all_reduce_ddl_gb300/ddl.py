@@ -146,8 +146,10 @@ def ddl_allreduce_bucket(plan, bucket, rank_bufs, scale, stream=None):
 
 
 def ddl_allreduce_host(plan, host_bufs, dev_bufs, scale, stream=None):
-    _ok(_lib.ddl_allreduce_host(plan, _ptr_array(_dev_ptrs(host_bufs)), _ptr_array(_dev_ptrs(dev_bufs)), scale,
-                                _stream_handle(stream)), "ddl_allreduce_host")
+    """dev_bufs None: the fused pass works on the host buffers in place."""
+    dev = None if dev_bufs is None else _ptr_array(_dev_ptrs(dev_bufs))
+    _ok(_lib.ddl_allreduce_host(plan, _ptr_array(_dev_ptrs(host_bufs)), dev, scale, _stream_handle(stream)),
+        "ddl_allreduce_host")
 
 
 def ddl_overlap_begin(plan, rank_bufs, scale, stream=None):

@@ -142,13 +142,21 @@ ddl_status_t ddl_allreduce(ddl_plan_t plan, void* const* rank_bufs, float scale,
 ddl_status_t ddl_allreduce_bucket(ddl_plan_t plan, int bucket, void* const* rank_bufs, float scale,
                                   void* stream);
 
-/* End-to-end form: copies P host buffers into the P device buffers, runs the
- * all-reduce, and copies the results back, all queued on stream.
- *  host_bufs: P host pointers (page-locked for asynchronous copies; pageable
- *    memory works but the copies then synchronize), N elements each, updated
- *    in place.  dev_bufs: P device buffers as for ddl_allreduce, owned by the
- *    caller.  The host buffers must stay valid until the stream reaches the
- *    end of the queued work. */
+/* End-to-end form for gradients held in host memory; the host buffers are
+ * updated in place.
+ *  host_bufs: P host pointers, N elements each.  They must stay valid until
+ *    the stream reaches the end of the queued work.
+ *  dev_bufs: P device buffers as for ddl_allreduce (caller-owned staging):
+ *    the call copies the host buffers in, all-reduces, and copies the results
+ *    back, pipelined over element ranges on the plan's own copy-in, compute
+ *    and copy-out streams (joined to `stream` at both ends).  Page-locked
+ *    host memory is needed for the copies to overlap.
+ *  dev_bufs == NULL: no staging.  The fused pass reads and writes the host
+ *    buffers directly over the host link.  They must be memory the GPU can
+ *    reach: page-locked (cudaHostAlloc / cudaHostRegister), managed, or
+ *    pageable on systems with coherent GPU access to pageable memory; other
+ *    memory returns DDL_ERR_INVALID_ARG.  Not available in stepwise mode
+ *    (DDL_ERR_UNSUPPORTED). */
 ddl_status_t ddl_allreduce_host(ddl_plan_t plan, void* const* host_bufs, void* const* dev_bufs, float scale,
                                 void* stream);
 

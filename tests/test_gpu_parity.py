@@ -232,6 +232,58 @@ def test_allreduce_host_buffers(ddl):
         assert np.array_equal(pinned[r].numpy(), ref[r])
 
 
+@pytest.mark.parametrize("case", [
+    dict(P=4, N=3_000_001, bucket_bytes=5_000_000),                       # 12 ranges over 3 buckets
+    dict(P=8, N=2_500_003, dtype="f16", topo="torus", X=4, Y=2),          # 5 ranges
+    dict(P=6, N=1_000_000, topo="multiring", k=2, mode="stepwise"),       # whole-bucket path
+])
+def test_allreduce_host_pipelined(ddl, case):
+    case = dict(case)
+    mode = case.pop("mode", "fused")
+    w = _w(seed=21, **case)
+    host = _host_inputs(w)
+    ref = [h.copy() for h in host]
+    oracle.emulate(oracle_cfg(w), ref, w.scale)
+    tdt = torch_dtype(w.dtype)
+    pinned = [torch.from_numpy(h.view(np.int16) if w.dtype == "f16" else h.copy()).clone().pin_memory()
+              for h in host]
+    dev = [torch.empty(w.N, dtype=tdt, device=DEV) for _ in range(w.P)]
+    with ddl.Plan.for_workload(w, mode=mode) as plan:
+        plan.allreduce_host(pinned, dev, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    for r in range(w.P):
+        got = pinned[r].numpy()
+        got = got.view(np.uint16) if w.dtype == "f16" else got
+        assert np.array_equal(got, ref[r]), r
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_allreduce_host_zero_copy(ddl, dtype):
+    """dev_bufs = NULL: the fused pass works on page-locked host memory in place."""
+    w = _w(P=8, N=400_003, dtype=dtype, topo="torus", X=4, Y=2, seed=31)
+    host = _host_inputs(w)
+    ref = [h.copy() for h in host]
+    oracle.emulate(oracle_cfg(w), ref, w.scale)
+    pinned = [torch.from_numpy(h.view(np.int16) if w.dtype == "f16" else h.copy()).clone().pin_memory()
+              for h in host]
+    with ddl.Plan.for_workload(w) as plan:
+        plan.allreduce_host(pinned, None, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+        for r in range(w.P):
+            got = pinned[r].numpy()
+            got = got.view(np.uint16) if w.dtype == "f16" else got
+            assert np.array_equal(got, ref[r]), r
+        # memory the GPU cannot reach is refused, unless the system gives it coherent access
+        plain = [np.zeros(w.N, dtype=np.float32 if dtype == "f32" else np.uint16) for _ in range(w.P)]
+        try:
+            plan.allreduce_host([a.ctypes.data for a in plain], None, w.scale)
+            torch.cuda.synchronize()
+        except ddl.DDLError as e:
+            assert e.status == ddl.DDL_ERR_INVALID_ARG
+
+
 def test_launch_counts_and_checks(ddl):
     w = _w(P=16, N=100_000, topo="torus", X=4, Y=4, bucket_bytes=100_000)
     bufs = device_bufs_generated(w, DEV)
