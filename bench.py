@@ -378,6 +378,12 @@ def main():
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = cpu_baseline(w)
 
+    # alpha-beta model of the same schedule on P real workers, at the Baidu
+    # write-up's ~6 GB/s InfiniBand (alpha 0) and with 10 us of latency per step
+    model = {"link_GBps": 6.0, "alpha0_s": round(plan.cost(0.0, 1 / 6e9), 6),
+             "alpha10us_s": round(plan.cost(10e-6, 1 / 6e9), 6), "steps": plan.traffic()[1],
+             "elements_sent_total": plan.traffic()[0]}
+
     if rank == 0:
         line = {"metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
@@ -389,6 +395,7 @@ def main():
                            "l2": f"inputs {w.P * w.N * w.esize / 1e9:.2f} GB per replica, larger than the 129 MB L2",
                            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU, P logical ranks"},
                 "clocks": clk, "gpu_launches": launches, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
+                "cluster_model": model,
                 "kernel_src": kernel_hash()}
         print(json.dumps(line), flush=True)
     plan.close()

@@ -531,6 +531,13 @@ ddl_status_t ddl_plan_traffic(ddl_plan_t p, uint64_t* moved, uint64_t* steps) {
   return DDL_OK;
 }
 
+ddl_status_t ddl_plan_cost(ddl_plan_t p, double alpha_s, double beta_s_per_byte, double* seconds) {
+  if (!p || !seconds || !(alpha_s >= 0.0) || !(beta_s_per_byte >= 0.0)) return DDL_ERR_INVALID_ARG;
+  *seconds = (double)p->tab.nsteps * alpha_s +
+             (double)p->tab.step_max_sum * (double)p->spec.esize * beta_s_per_byte;
+  return DDL_OK;
+}
+
 ddl_status_t ddl_plan_fold_order(ddl_plan_t p, size_t i, int32_t* order, int32_t* inner, int32_t* groups) {
   if (!p || !order || !inner || !groups) return DDL_ERR_INVALID_ARG;
   if (p->spec.mode == ddl::kStepwise) return DDL_ERR_UNSUPPORTED;

@@ -134,9 +134,11 @@ struct Builder {
 
   // ---- message lists of the step-by-step schedule ----
   std::vector<Xfer> cur;
+  uint64_t step_max = 0;  // largest message of the step being built
 
   void msg(uint64_t lo, uint64_t len, int src, int dst, uint32_t op) {
     t->moved += (op == kScaleOnly) ? 0 : len;
+    if (op != kScaleOnly && len > step_max) step_max = len;
     if (!with_steps) return;
     Xfer x{};
     x.lo = lo;
@@ -163,7 +165,11 @@ struct Builder {
     }
   }
   void close_step(bool communication) {
-    if (communication) ++t->nsteps;
+    if (communication) {
+      ++t->nsteps;
+      t->step_max_sum += step_max;
+    }
+    step_max = 0;
     if (!with_steps) return;
     Step st{};
     st.xfer_begin = (uint32_t)t->xfers.size();

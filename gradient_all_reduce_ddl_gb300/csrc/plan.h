@@ -90,6 +90,7 @@ struct Tables {
   std::vector<Step> steps;
   uint64_t moved = 0;   // elements sent over all messages
   uint64_t nsteps = 0;  // sequential communication steps
+  uint64_t step_max_sum = 0;  // sum over steps of the step's largest message (elements)
 };
 
 // Returns "" if the spec is valid, else a reason.  unsupported is set when the

@@ -38,6 +38,7 @@ EXPORTS = [
     "ddl_allreduce_bucket", "ddl_allreduce_host", "ddl_overlap_begin", "ddl_bucket_ready", "ddl_overlap_end",
     "ddl_plan_num_buckets", "ddl_plan_bucket_range", "ddl_plan_traffic", "ddl_plan_fold_order",
     "ddl_plan_launches", "ddl_plan_check", "ddl_status_string", "ddl_plan_destroy", "ddl_allreduce_noalloc",
+    "ddl_plan_cost",
 ]
 
 
@@ -69,6 +70,7 @@ _sig("ddl_overlap_end", _i, _vp, _vp)
 _sig("ddl_plan_num_buckets", _i, _vp, _P(_i))
 _sig("ddl_plan_bucket_range", _i, _vp, _i, _P(_sz), _P(_sz))
 _sig("ddl_plan_traffic", _i, _vp, _P(_u64), _P(_u64))
+_sig("ddl_plan_cost", _i, _vp, ctypes.c_double, ctypes.c_double, _P(ctypes.c_double))
 _sig("ddl_plan_fold_order", _i, _vp, _sz, _P(ctypes.c_int32), _P(ctypes.c_int32), _P(ctypes.c_int32))
 _sig("ddl_plan_launches", _i, _vp, _P(_u64))
 _sig("ddl_plan_check", _i, _vp)
@@ -183,6 +185,12 @@ def ddl_plan_traffic(plan):
     return m.value, s.value
 
 
+def ddl_plan_cost(plan, alpha_s, beta_s_per_byte):
+    t = ctypes.c_double()
+    _ok(_lib.ddl_plan_cost(plan, alpha_s, beta_s_per_byte, ctypes.byref(t)), "ddl_plan_cost")
+    return t.value
+
+
 def ddl_plan_fold_order(plan, i, P):
     order = (ctypes.c_int32 * P)()
     inner, groups = ctypes.c_int32(), ctypes.c_int32()
@@ -290,6 +298,10 @@ class Plan:
 
     def fold_order(self, i):
         return ddl_plan_fold_order(self.handle, i, self.P)
+
+    def cost(self, alpha_s, beta_s_per_byte):
+        """alpha-beta model of this schedule on P real workers (seconds)."""
+        return ddl_plan_cost(self.handle, alpha_s, beta_s_per_byte)
 
     @property
     def launches(self):

@@ -207,6 +207,18 @@ ddl_status_t ddl_plan_bucket_range(ddl_plan_t plan, int bucket, size_t* begin, s
  * 2(X-1)+2(Y-1), per bucket).  Host-only. */
 ddl_status_t ddl_plan_traffic(ddl_plan_t plan, uint64_t* elems_moved_total, uint64_t* steps);
 
+/* alpha-beta cost of the schedule on a cluster of P real workers: every
+ * communication step costs alpha_s (latency) plus beta_s_per_byte times the
+ * bytes of the step's largest message (each worker sends one message per step
+ * on its own link, all at once); the all-reduce costs the sum over its steps
+ * and buckets.  Ring: 2(P-1)(alpha + (n/P)e beta); torus: 2(X-1)(alpha +
+ * (n/X)e beta) + 2(Y-1)(alpha + (n/(XY))e beta).  This is the latency /
+ * bandwidth trade-off that "[论文解读] PowerAI DDL" (abstract) names for its
+ * multi-ring pattern; the Baidu write-up's example (1.2 GB gradient, about
+ * 6 GB/s InfiniBand, about 400 ms per iteration) is this model with
+ * alpha = 0.  Host-only.  alpha_s, beta_s_per_byte >= 0. */
+ddl_status_t ddl_plan_cost(ddl_plan_t plan, double alpha_s, double beta_s_per_byte, double* seconds);
+
 /* Introspection: the fold order of element i as the plan's tables hold it:
  * order[0..P-1] = ranks in the order they are added, *inner = group length
  * (X for the torus, else P), *groups = Y for the torus, else 1.  Host-only. */

@@ -14,6 +14,7 @@ Parity status per function:
   buckets       pinned (hand-computed layer packing, closed form of fixed buckets)
   f32_to_f16    pinned (exhaustive against numpy's and the C compiler's binary16)
   ref64         pinned (integer inputs: exact sums)
+  cost          pinned (closed forms; the 400 ms language-model example)
 
 Buffers are numpy arrays: float32 for fp32, uint16 bit patterns for fp16.
 """
@@ -82,6 +83,8 @@ def _load():
             lib.oracle_ring_strides.restype = ctypes.c_int
             lib.oracle_ref64.argtypes = [i32, u64, i32, P, ctypes.c_double, P]
             lib.oracle_ref64.restype = None
+            lib.oracle_cost.argtypes = [cfgp, ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
+            lib.oracle_cost.restype = ctypes.c_int
             lib.oracle_f32_to_f16.argtypes = [P, P, u64]
             lib.oracle_f16_to_f32.argtypes = [P, P, u64]
             lib.oracle_f32_pattern_to_f16.argtypes = [u64, u64, P]
@@ -150,6 +153,15 @@ def emulate(cfg: Config, bufs, scale: float, stop_after: int = -1):
 def traffic(cfg: Config):
     """Elements moved and steps, counted by the emulation without data."""
     return emulate(cfg, None, 1.0)
+
+
+def cost(cfg: Config, alpha: float, beta: float) -> float:
+    """alpha-beta seconds of the schedule on P real workers (per-step largest
+    message, steps in sequence)."""
+    lib = _load()
+    t = ctypes.c_double()
+    _check(lib.oracle_cost(cfg._ref(), alpha, beta, ctypes.byref(t)))
+    return t.value
 
 
 def closed_form(cfg: Config, x_rows: np.ndarray, idx: np.ndarray, scale: float) -> np.ndarray:

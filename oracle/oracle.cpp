@@ -235,6 +235,7 @@ struct Emu {
   float scale;
   int64_t stop_after; /* number of steps to run; < 0 = all */
   uint64_t moved = 0, steps = 0;
+  uint64_t step_max_sum = 0; /* sum over steps of the largest message (elements) */
   bool stopped = false;
   std::vector<Msg> pending;
 
@@ -285,8 +286,10 @@ struct Emu {
       pending.clear();
       return;
     }
+    uint64_t biggest = 0;
     for (Msg& g : pending) {
       moved += g.hi - g.lo;
+      if (g.hi - g.lo > biggest) biggest = g.hi - g.lo;
       if (!b) continue;
       g.data.resize(g.hi - g.lo);
       for (uint64_t i = g.lo; i < g.hi; ++i) g.data[i - g.lo] = b->raw(g.src, i);
@@ -304,6 +307,7 @@ struct Emu {
     }
     pending.clear();
     ++steps;
+    step_max_sum += biggest;
   }
 
   void ring_bucket(uint64_t lo, uint64_t hi) {
@@ -490,6 +494,19 @@ int oracle_emulate(const oracle_cfg* cfg, void* const* bufs, float scale, int64_
   e.run();
   if (elems_moved) *elems_moved = e.moved;
   if (steps) *steps = e.steps;
+  return 0;
+}
+
+/* alpha-beta time of the schedule on P real workers: each step costs
+ * alpha + beta * (bytes of its largest message), all ranks sending at once;
+ * steps add up.  From the emulation's own message lists. */
+int oracle_cost(const oracle_cfg* cfg, double alpha, double beta, double* seconds) {
+  Cfg c;
+  const int rc = load_cfg(cfg, c);
+  if (rc) return rc;
+  Emu e(c, nullptr, 1.0f, -1);
+  e.run();
+  *seconds = (double)e.steps * alpha + (double)e.step_max_sum * (double)c.esize() * beta;
   return 0;
 }
 

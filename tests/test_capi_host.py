@@ -79,6 +79,16 @@ def test_tables_match_oracle(ddl, case):
             assert (l_ord, l_in, l_gr) == (o_ord.tolist(), o_in, o_gr), i
 
 
+@pytest.mark.parametrize("case", CASES)
+def test_cost_model_matches_oracle(ddl, case):
+    plan, cfg = _pair(**case)
+    with plan:
+        for a, b in [(0.0, 1e-9), (2e-6, 0.0), (3e-6, 1.6e-10)]:
+            assert plan.cost(a, b) == pytest.approx(oracle.cost(cfg, a, b), rel=1e-12, abs=1e-18)
+        with pytest.raises(ddl.DDLError):
+            plan.cost(-1.0, 0.0)
+
+
 @pytest.mark.parametrize("name", ["torus4x4_resnet50", "torus8x4_resnet50_f16", "multiring64_resnet101",
                                   "ring16_lm300m", "torus4x4_lm300m"])
 def test_workload_tables_match_oracle(ddl, name):

@@ -293,6 +293,33 @@ def test_page3_traffic_figure(oracle_lib):
     assert (ring_steps, torus_steps) == (30, 12)
 
 
+def test_cost_model_closed_forms_and_page3_figure(oracle_lib):
+    """alpha-beta cost from the emulation's own message lists.
+    Baidu write-up, the 300M-parameter language model: a 1.2 GB gradient over
+    ~6 GB/s InfiniBand takes about 2.4 GB / 6 GB/s = 400 ms per iteration."""
+    beta = 1 / 6e9
+    t40 = oracle.cost(oracle.Config(P=40, N=300_000_000), 0.0, beta)
+    assert t40 == pytest.approx(2 * 39 / 40 * 1.2e9 / 6e9)        # 0.39 s
+    assert abs(t40 - 0.400) / 0.400 < 0.03
+    assert oracle.cost(oracle.Config(P=4000, N=300_000_000), 0.0, beta) == pytest.approx(0.4, rel=1e-3)
+    # closed forms (n divisible): ring 2(P-1)(a + n/P e b); torus 2(X-1)(a + n/X e b) + 2(Y-1)(a + n/XY e b)
+    a, b, n = 5e-6, 1e-10, 96_000
+    assert oracle.cost(oracle.Config(P=16, N=n), a, b) == pytest.approx(30 * (a + n / 16 * 4 * b))
+    assert oracle.cost(oracle.Config(P=16, N=n, topo="torus", X=4, Y=4), a, b) == \
+        pytest.approx(6 * (a + n / 4 * 4 * b) + 6 * (a + n / 16 * 4 * b))
+    assert oracle.cost(oracle.Config(P=16, N=n, topo="multiring", k=2), a, b) == \
+        pytest.approx(30 * (a + n / 32 * 4 * b))
+    # fp16 halves the bandwidth term
+    assert oracle.cost(oracle.Config(P=8, N=n, dtype="f16"), 0.0, b) == pytest.approx(14 * n / 8 * 2 * b)
+    # the torus keeps the ring's bandwidth term, 2(X-1)/X + 2(Y-1)/XY = 2(P-1)/P
+    # (both bandwidth-optimal), and cuts the steps from 30 to 12
+    ring = oracle.Config(P=16, N=n)
+    torus = oracle.Config(P=16, N=n, topo="torus", X=4, Y=4)
+    assert oracle.cost(torus, 0.0, b) == pytest.approx(oracle.cost(ring, 0.0, b))
+    assert oracle.cost(torus, 1e-3, 0.0) == pytest.approx(12e-3)
+    assert oracle.cost(ring, 1e-3, 0.0) == pytest.approx(30e-3)
+
+
 # --------------------------------------------------------------------------
 # Special cases that reduce to a simpler schedule or a plain operation
 # --------------------------------------------------------------------------
