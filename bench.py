@@ -167,6 +167,24 @@ def smi_gpu_id(local: int) -> str:
     return str(local)
 
 
+def reduce_max(x: float, ws: int) -> float:
+    """Largest value over the ranks (the job's time is its slowest replica)."""
+    if ws <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_replica_step: int, ws: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every replica moves its own bytes each step, and
+    the step takes the slowest replica's time."""
+    return bytes_per_replica_step * ws / (ms_per_step * 1e-3) / 1e9
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -296,14 +314,10 @@ def main():
     clocks.mark("t1")
     clk = clocks.stop()
     launches = plan.launches - launches0 if graph is None else graph_launches * args.steps
-    total_ms = start.elapsed_time(end)
+    total_ms = reduce_max(start.elapsed_time(end), ws)
     per_call_ms = [a.elapsed_time(b) for a, b in ev]
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    gbs = nbytes * ws / (ms_per_step * 1e-3) / 1e9
+    gbs = job_gbs(nbytes, ws, ms_per_step)
     elems = w.P * w.N * ws / (ms_per_step * 1e-3)
 
     # roofline of the dominant kernel: one fused launch per bucket
@@ -341,12 +355,8 @@ def main():
             plan.allreduce_host(host, bufs, w.scale, stream)
         s1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = s0.elapsed_time(s1) / args.e2e_steps
-        te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        if ws > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e_ms = float(te.item())
-        staged = {"value": round(nbytes * ws / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e2e_ms = reduce_max(s0.elapsed_time(s1) / args.e2e_steps, ws)
+        staged = {"value": round(job_gbs(nbytes, ws, e2e_ms), 2), "unit": "GB/s",
                   "h2d_bytes_per_step": w.P * w.N * w.esize, "d2h_bytes_per_step": w.P * w.N * w.esize,
                   "ms_per_step": round(e2e_ms, 3), "steps": args.e2e_steps,
                   "path": "ddl_allreduce_host with device staging: copy-in, fused pass, copy-out "
@@ -360,12 +370,8 @@ def main():
             plan.allreduce_host(host, None, w.scale, stream)
         s1.record(stream)
         torch.cuda.synchronize(dev)
-        zc_ms = s0.elapsed_time(s1) / args.e2e_steps
-        tz = torch.tensor([zc_ms], dtype=torch.float64, device=dev)
-        if ws > 1:
-            dist.all_reduce(tz, op=dist.ReduceOp.MAX)
-        zc_ms = float(tz.item())
-        zero = {"value": round(nbytes * ws / (zc_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        zc_ms = reduce_max(s0.elapsed_time(s1) / args.e2e_steps, ws)
+        zero = {"value": round(job_gbs(nbytes, ws, zc_ms), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": w.P * w.N * w.esize, "d2h_bytes_per_step": w.P * w.N * w.esize,
                 "ms_per_step": round(zc_ms, 3), "steps": args.e2e_steps,
                 "path": "ddl_allreduce_host without staging: the fused pass loads and stores the page-locked "
