@@ -42,6 +42,7 @@ DEFAULT_WORKLOAD = "torus4x4_resnet50"
 # kernel source it was taken on).  A changed kernel reports null.
 NCU_TRAFFIC = {
     ("torus4x4_resnet50", "ldg", "0e52a75d29912526"): 1_635_956_224 + 1_575_996_160,
+    ("torus4x4_resnet50", "ldg", "114f33c52577cd67"): 1_635_897_344 + 1_575_593_472,
 }
 
 KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]
@@ -185,6 +186,70 @@ def job_gbs(bytes_per_replica_step: int, ws: int, ms_per_step: float) -> float:
     return bytes_per_replica_step * ws / (ms_per_step * 1e-3) / 1e9
 
 
+def overlap_study(plan, bufs, w, stream, steps: int = 20, tokens: int = 2048):
+    """Back-propagation overlapped with the bucketed all-reduce (Baidu
+    write-up, opening paragraphs): a synthetic backward produces the buckets'
+    gradients in reverse-layer order on `stream` -- per bucket a bf16 GEMM of
+    2*tokens*params flops and the write of the bucket's
+    gradients into all P rank buffers -- and either (a) all-reduces after the
+    whole backward, or (b) signals each finished bucket (ddl_bucket_ready) so
+    the plan's side stream reduces it while the next bucket is computed."""
+    import torch
+    nb = plan.num_buckets
+    ranges = plan.buckets()
+    dev = bufs[0].device
+    pristine = [b.clone() for b in bufs]
+    gemms = []
+    for lo, hi in ranges:
+        n = max(64, ((hi - lo) // 4096 + 63) // 64 * 64)
+        gemms.append((torch.randn(tokens, 4096, device=dev, dtype=torch.bfloat16),
+                      torch.randn(4096, n, device=dev, dtype=torch.bfloat16)))
+
+    def backward_bucket(b):
+        a, m = gemms[b]
+        torch.matmul(a, m)
+        lo, hi = ranges[b]
+        for r in range(w.P):
+            bufs[r][lo:hi].copy_(pristine[r][lo:hi])
+
+    def seq():
+        for b in range(nb):
+            backward_bucket(b)
+        plan.allreduce(bufs, w.scale, stream)
+
+    def ovl():
+        plan.overlap_begin(bufs, w.scale, stream)
+        for b in range(nb):
+            backward_bucket(b)
+            plan.bucket_ready(b, stream)
+        plan.overlap_end(stream)
+
+    def backward_only():
+        for b in range(nb):
+            backward_bucket(b)
+
+    out = {}
+    with torch.cuda.stream(stream):
+        for name, fn in [("backward_only", backward_only), ("sequential", seq), ("overlapped", ovl)]:
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize(dev)
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(steps):
+                fn()
+            s1.record(stream)
+            torch.cuda.synchronize(dev)
+            out[name + "_ms"] = round(s0.elapsed_time(s1) / steps, 4)
+    out["allreduce_alone_ms"] = None
+    out["saved_ms"] = round(out["sequential_ms"] - out["overlapped_ms"], 4)
+    out["buckets"] = nb
+    out["backward"] = (f"per bucket: bf16 GEMM {tokens}x4096 @ 4096x(params/4096) + gradient writes to all "
+                       f"P ranks")
+    del pristine, gemms
+    return out
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -239,6 +304,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--overlap", action="store_true",
+                    help="also time a synthetic backward overlapped with the bucketed all-reduce")
+    ap.add_argument("--overlap-tokens", type=int, default=2048,
+                    help="GEMM rows of the synthetic backward (its compute per parameter)")
     ap.add_argument("--graph", action="store_true",
                     help="capture one ddl_allreduce in a CUDA graph and replay it each step")
     args = ap.parse_args()
@@ -380,6 +449,11 @@ def main():
         e2e = dict(e2e, other_path=alt)
         del host
 
+    overlap = None
+    if args.overlap:
+        overlap = overlap_study(plan, bufs, w, stream, tokens=args.overlap_tokens)
+        overlap["allreduce_alone_ms"] = round(ms_per_step, 4)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = cpu_baseline(w)
@@ -401,7 +475,7 @@ def main():
                            "l2": f"inputs {w.P * w.N * w.esize / 1e9:.2f} GB per replica, larger than the 129 MB L2",
                            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU, P logical ranks"},
                 "clocks": clk, "gpu_launches": launches, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
-                "cluster_model": model,
+                "cluster_model": model, "overlap": overlap,
                 "kernel_src": kernel_hash()}
         print(json.dumps(line), flush=True)
     plan.close()
