@@ -83,6 +83,27 @@ ddl_status_t cuda_status(cudaError_t e) {
   return e == cudaErrorMemoryAllocation ? DDL_ERR_OOM : DDL_ERR_CUDA;
 }
 
+// n-D torus plans fold through the level cascade; others use each
+// segment's (inner, groups).
+void set_levels(const ddl_plan* p, ddl::FoldParams* fp) {
+  if (p->spec.topo != ddl::kTorusND) return;
+  fp->nlev = (int32_t)p->spec.dims.size();
+  fp->top = -1;
+  for (int l = 0; l < fp->nlev; ++l) {
+    fp->lev[l] = (uint16_t)p->spec.dims[l];
+    if (p->spec.dims[l] > 1) fp->top = l;
+  }
+}
+
+// Work-item size for the plan's kernel: the n-D pass takes one column per
+// thread (<= 4 KB per rank); the staged passes fill ~64 KB per stage.
+uint32_t choose_tile(const Spec& s, int kernel) {
+  const uint32_t ldg = ddl::ldg_tile_bytes(s.N * (uint64_t)s.esize);
+  if (s.topo == ddl::kTorusND) return ldg < 4096u ? ldg : 4096u;
+  if (kernel == DDL_KERNEL_BULK || kernel == DDL_KERNEL_BULK_LOAD) return ddl::bulk_tile_bytes(s.P);
+  return ldg;
+}
+
 // Binds the plan to the current device and makes its device tables current.
 ddl_status_t ensure_device(ddl_plan* p) {
   int dev = -1;
@@ -196,6 +217,7 @@ ddl_status_t run_bucket(ddl_plan* p, int b, void* const* bufs, bool aligned, flo
   if (n == 0) return DDL_OK;
   fp.n_items = n;
   fp.tile_bytes = p->spec.tile_bytes;
+  set_levels(p, &fp);
   const cudaError_t e = ddl::launch_fold(fp, n, f16, variant, s);
   if (e != cudaSuccess) return cuda_status(e);
   ++p->launches;
@@ -226,6 +248,7 @@ ddl_status_t run_items(ddl_plan* p, uint32_t ia, uint32_t ib, void* const* bufs,
   if (aligned && p->kernel == DDL_KERNEL_BULK_LOAD) variant = ddl::kVarBulkLoad;
   fp.n_items = ib - ia;
   fp.tile_bytes = p->spec.tile_bytes;
+  set_levels(p, &fp);
   const cudaError_t e = ddl::launch_fold(fp, ib - ia, f16, variant, s);
   if (e != cudaSuccess) return cuda_status(e);
   ++p->launches;
@@ -323,11 +346,31 @@ ddl_status_t ddl_plan_set_mode(ddl_plan_t p, ddl_mode_t mode) {
   return st;
 }
 
+ddl_status_t ddl_plan_set_torus_dims(ddl_plan_t p, int ndims, const int* dims) {
+  if (!p || p->ov_active || ndims < 1 || ndims > ddl::kMaxDims || !dims) return DDL_ERR_INVALID_ARG;
+  Spec s = p->spec;
+  s.topo = ddl::kTorusND;
+  s.dims.assign(dims, dims + ndims);
+  while (s.dims.size() > 1 && s.dims.back() == 1) s.dims.pop_back();  // no steps along them
+  s.k = 1;
+  s.X = s.Y = 0;
+  s.tile_bytes = choose_tile(s, p->kernel);
+  bool unsupported = false;
+  const std::string why = ddl::validate(s, &unsupported);
+  if (!why.empty()) return unsupported ? DDL_ERR_UNSUPPORTED : DDL_ERR_INVALID_ARG;
+  const Spec old = p->spec;
+  p->spec = s;
+  const ddl_status_t st = rebuild(p);
+  if (st != DDL_OK) {
+    p->spec = old;
+    rebuild(p);
+  }
+  return st;
+}
+
 ddl_status_t ddl_plan_set_kernel(ddl_plan_t p, ddl_kernel_t k) {
   if (!p || p->ov_active || k < DDL_KERNEL_AUTO || k > DDL_KERNEL_BULK_LOAD) return DDL_ERR_INVALID_ARG;
-  const bool staged = k == DDL_KERNEL_BULK || k == DDL_KERNEL_BULK_LOAD;
-  const uint32_t tile = staged ? ddl::bulk_tile_bytes(p->spec.P)
-                               : ddl::ldg_tile_bytes(p->spec.N * (uint64_t)p->spec.esize);
+  const uint32_t tile = choose_tile(p->spec, (int)k);
   p->kernel = (int)k;
   if (tile == p->spec.tile_bytes) return DDL_OK;
   const Spec old = p->spec;

@@ -17,6 +17,8 @@
 // so the compiler cannot contract or reorder them.
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "kernels.h"
 
 namespace ddl {
@@ -260,6 +262,125 @@ __global__ void __launch_bounds__(kThreads, MINB) fold_ldg_kernel(const __grid_c
   if (threadIdx.x < nh + nt) {
     const uint64_t e = threadIdx.x < nh ? eb + threadIdx.x : ve * L + (threadIdx.x - nh);
     fold_scalar<F16>(s_ptr, e, P, inner, groups, rh, p.scale);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// n-D torus register pass: the fold is d nested left folds (innermost over
+// dim 0 from chunk c_0, then dim 1, ...).  A cascade of one accumulator per
+// level follows the ranks in fold order: a finished group of level l is added
+// into level l+1.  Every add is rounded to binary16 where a hop would carry
+// it, except the final add (the last one at the highest level of size > 1).
+// One column per thread (fp16 keeps 4 levels x 8 lanes of accumulators), so
+// the plan's items are at most 4 KB per rank.
+// ---------------------------------------------------------------------------
+// One accumulator per level (levels written out, so every index is a
+// compile-time constant and the accumulators live in registers); NL lanes.
+template <int NL>
+struct Cascade {
+  float a0[NL], a1[NL], a2[NL], a3[NL];
+  int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+
+  // cur into level acc (first of its group: copy; else add, rounded unless final)
+  __device__ __forceinline__ static void add(float* acc, const float* cur, bool first, bool round) {
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+      if (first) {
+        acc[l] = cur[l];
+      } else {
+        const float s = __fadd_rn(acc[l], cur[l]);
+        acc[l] = round ? round_h(s) : s;
+      }
+    }
+  }
+  // one value at fold position t (last = t is the final position); returns
+  // after the first level whose group is still open
+  __device__ __forceinline__ void push(const float* v, bool last, const FoldParams& p, bool rh) {
+    add(a0, v, c0 == 0, rh && !(last && p.top == 0));
+    if (++c0 < (int)p.lev[0]) return;
+    c0 = 0;
+    if (p.nlev < 2) return;
+    add(a1, a0, c1 == 0, rh && !(last && p.top == 1));
+    if (++c1 < (int)p.lev[1]) return;
+    c1 = 0;
+    if (p.nlev < 3) return;
+    add(a2, a1, c2 == 0, rh && !(last && p.top == 2));
+    if (++c2 < (int)p.lev[2]) return;
+    c2 = 0;
+    if (p.nlev < 4) return;
+    add(a3, a2, c3 == 0, rh && !(last && p.top == 3));
+    if (++c3 < (int)p.lev[3]) return;
+    c3 = 0;
+  }
+  // the outermost level's value
+  __device__ __forceinline__ void result(float* out, int nlev) const {
+#pragma unroll
+    for (int l = 0; l < NL; ++l) out[l] = nlev == 1 ? a0[l] : nlev == 2 ? a1[l] : nlev == 3 ? a2[l] : a3[l];
+  }
+};
+
+template <bool F16>
+__device__ __forceinline__ void fold_nd_scalar(const FoldParams& p, char* const* ptr, uint64_t e, bool rh) {
+  Cascade<1> cs;
+  for (int t = 0; t < p.P; ++t) {
+    const float v = load_elem<F16>(ptr[t], e);
+    cs.push(&v, t == p.P - 1, p, rh);
+  }
+  float fin;
+  cs.result(&fin, p.nlev);
+  const float r = __fmul_rn(fin, p.scale);
+  for (int t = 0; t < p.P; ++t) store_elem<F16>(ptr[t], e, r);
+}
+
+template <bool F16, int B>
+__global__ void __launch_bounds__(kThreads, 2) fold_nd_kernel(const __grid_constant__ FoldParams p) {
+  constexpr int L = F16 ? 8 : 4;
+  __shared__ char* s_ptr[kMaxP];
+  __shared__ Item s_item;
+  __shared__ Segment s_seg;
+  __shared__ int s_ok;
+  if (!load_item(p, s_ptr, &s_item, &s_seg, &s_ok)) return;
+  const int P = p.P;
+  const bool rh = F16 && p.round_hops;
+  const uint64_t eb = s_item.begin, ee = eb + s_item.len;
+  const uint64_t vb = (eb + L - 1) / L, ve = ee / L;
+
+  if (!p.vector_ok || vb >= ve) {
+    for (uint64_t e = eb + threadIdx.x; e < ee; e += kThreads) fold_nd_scalar<F16>(p, s_ptr, e, rh);
+    return;
+  }
+  if (ve - vb > (uint64_t)kThreads) {  // one column per thread: items must be <= 4 KB per rank
+    if (threadIdx.x == 0) atomicOr(p.err, kErrBadItem);
+    return;
+  }
+  const uint64_t col = vb + threadIdx.x;
+  if (col < ve) {
+    Cascade<L> cs;
+    for (int t0 = 0; t0 < P; t0 += B) {
+      uint4 raw[B];
+#pragma unroll
+      for (int j = 0; j < B; ++j)
+        if (t0 + j < P) raw[j] = __ldcs(reinterpret_cast<const uint4*>(s_ptr[t0 + j]) + col);
+#pragma unroll
+      for (int j = 0; j < B; ++j) {
+        if (t0 + j < P) {
+          float f[L];
+          unpack<F16>(raw[j], f);
+          cs.push(f, t0 + j == P - 1, p, rh);
+        }
+      }
+    }
+    float r[L];
+    cs.result(r, p.nlev);
+#pragma unroll
+    for (int l = 0; l < L; ++l) r[l] = __fmul_rn(r[l], p.scale);
+    const uint4 res = pack<F16>(r);
+    for (int t = 0; t < P; ++t) __stcs(reinterpret_cast<uint4*>(s_ptr[t]) + col, res);
+  }
+  const uint64_t nh = vb * L - eb, nt = ee - ve * L;
+  if (threadIdx.x < nh + nt) {
+    const uint64_t e = threadIdx.x < nh ? eb + threadIdx.x : ve * L + (threadIdx.x - nh);
+    fold_nd_scalar<F16>(p, s_ptr, e, rh);
   }
 }
 
@@ -597,6 +718,11 @@ cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t strea
 
 cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream) {
   if (n_items == 0) return cudaSuccess;
+  if (p.nlev > 0) {  // n-D torus: the level-cascade register pass
+    if (f16) fold_nd_kernel<true, 8><<<n_items, kThreads, 0, stream>>>(p);
+    else fold_nd_kernel<false, 8><<<n_items, kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
   if (variant == kVarBulk)
     return f16 ? launch_bulk<true, true>(p, n_items, stream) : launch_bulk<false, true>(p, n_items, stream);
   if (variant == kVarBulkLoad)

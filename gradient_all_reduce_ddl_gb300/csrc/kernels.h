@@ -31,7 +31,10 @@ struct FoldParams {
   int32_t vector_ok;   // every rank pointer is 16-byte aligned
   uint32_t n_items;    // items in this launch (persistent kernels)
   uint32_t tile_bytes; // bytes per rank of the largest item
-  uint32_t pad;
+  int32_t nlev;        // n-D torus: fold levels (0 = use each segment's inner/groups)
+  uint16_t lev[kMaxDims];  // level sizes, innermost first (the torus dims)
+  int32_t top;         // highest level of size > 1 (its last add is the final one)
+  int32_t pad2;
   void* bufs[kMaxP];   // rank r's buffer
 };
 

@@ -121,6 +121,10 @@ struct Builder {
       }
       return;
     }
+    if (s.topo == kTorusND) {
+      nd_segments(b.lo, n, 0, std::vector<int>(s.dims.size(), 0), order);
+      return;
+    }
     const int X = s.X, Y = s.Y;
     for (int c = 0; c < X; ++c) {
       const uint64_t clo = b.lo + part_lo(n, X, c), cn = part_len(n, X, c);
@@ -129,6 +133,31 @@ struct Builder {
           for (int h = 0; h < X; ++h) order[g * X + h] = ((d + g) % Y) * X + (c + h) % X;
         add_segment(clo + part_lo(cn, Y, d), part_len(cn, Y, d), order, X, Y);
       }
+    }
+  }
+
+  // n-D torus: the range [lo, lo+n) is split along dim k into D_k chunks;
+  // chunk tuple (c_0..c_{d-1}) folds, innermost first, the ranks with
+  // coordinates x_k = (c_k + g_k) mod D_k for g_k = 0..D_k-1.
+  void nd_segments(uint64_t lo, uint64_t n, int k, std::vector<int> ch, std::vector<int>& order) {
+    const int d = (int)s.dims.size();
+    if (k == d) {
+      for (int t = 0; t < s.P; ++t) {
+        int rest = t, r = 0, stride = 1;
+        for (int j = 0; j < d; ++j) {
+          const int g = rest % s.dims[j];
+          rest /= s.dims[j];
+          r += ((ch[j] + g) % s.dims[j]) * stride;
+          stride *= s.dims[j];
+        }
+        order[t] = r;
+      }
+      add_segment(lo, n, order, s.dims[0], s.P / s.dims[0]);
+      return;
+    }
+    for (int c = 0; c < s.dims[k]; ++c) {
+      ch[k] = c;
+      nd_segments(lo + part_lo(n, s.dims[k], c), part_len(n, s.dims[k], c), k + 1, ch, order);
     }
   }
 
@@ -208,6 +237,10 @@ struct Builder {
       }
       return;
     }
+    if (s.topo == kTorusND) {
+      nd_steps(b);
+      return;
+    }
     const int X = s.X, Y = s.Y;
     std::vector<std::vector<int>> row(Y, std::vector<int>(X)), col(X, std::vector<int>(Y));
     for (int y = 0; y < Y; ++y)
@@ -229,6 +262,61 @@ struct Builder {
     for (int st = 0; st < X - 1; ++st) {
       for (int y = 0; y < Y; ++y) ag(row[y], b.lo, n, st);
       close_step(true);
+    }
+  }
+
+  // n-D torus steps: reduce-scatter along dims 0..d-2 (each line of D_k ranks
+  // on the range it has reduced so far), all-reduce along dim d-1, then
+  // all-gather along dims d-2..0.  After the reduce-scatter along dim j a
+  // rank at x_j holds part (x_j + 1) mod D_j of the range it started with.
+  void nd_range(int r, int k, uint64_t lo, uint64_t n, uint64_t* a, uint64_t* m) const {
+    uint64_t st = lo, len = n;
+    for (int j = 0; j < k; ++j) {
+      const int x = r % s.dims[j];
+      r /= s.dims[j];
+      const uint64_t part = (uint64_t)((x + 1) % s.dims[j]);
+      st += part_lo(len, s.dims[j], part);
+      len = part_len(len, s.dims[j], part);
+    }
+    *a = st;
+    *m = len;
+  }
+  std::vector<std::vector<int>> nd_lines(int k) const {
+    std::vector<std::vector<int>> out;
+    int stride = 1;
+    for (int j = 0; j < k; ++j) stride *= s.dims[j];
+    for (int r = 0; r < s.P; ++r) {
+      if ((r / stride) % s.dims[k] != 0) continue;
+      std::vector<int> line(s.dims[k]);
+      for (int t = 0; t < s.dims[k]; ++t) line[t] = r + t * stride;
+      out.push_back(line);
+    }
+    return out;
+  }
+  void nd_steps(const Bucket& b) {
+    const int d = (int)s.dims.size();
+    const uint64_t n = b.hi - b.lo;
+    for (int k = 0; k < d; ++k) {
+      const auto lines = nd_lines(k);
+      for (int st = 0; st < s.dims[k] - 1; ++st) {
+        for (const auto& line : lines) {
+          uint64_t a, m;
+          nd_range(line[0], k, b.lo, n, &a, &m);
+          rs(line, a, m, st, k == d - 1);
+        }
+        close_step(true);
+      }
+    }
+    for (int k = d - 1; k >= 0; --k) {
+      const auto lines = nd_lines(k);
+      for (int st = 0; st < s.dims[k] - 1; ++st) {
+        for (const auto& line : lines) {
+          uint64_t a, m;
+          nd_range(line[0], k, b.lo, n, &a, &m);
+          ag(line, a, m, st);
+        }
+        close_step(true);
+      }
     }
   }
 };
@@ -277,6 +365,15 @@ std::string validate(const Spec& s, bool* unsupported) {
     }
   } else if (s.topo == kTorus) {
     if (s.X < 1 || s.Y < 1 || (int64_t)s.X * s.Y != s.P) return "torus needs X * Y == P";
+  } else if (s.topo == kTorusND) {
+    if (s.dims.empty() || (int)s.dims.size() > kMaxDims) return "n-D torus needs 1..4 dims";
+    int64_t prod = 1;
+    for (int d : s.dims) {
+      if (d < 1) return "n-D torus dims must be >= 1";
+      prod *= d;
+    }
+    if (prod != s.P) return "n-D torus dims must multiply to P";
+    if (s.dims.size() > 1 && s.dims.back() == 1) return "trailing dims of size 1 must be dropped";
   } else if (s.topo != kRing) {
     return "unknown topology kind";
   }

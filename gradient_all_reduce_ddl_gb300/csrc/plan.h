@@ -57,7 +57,8 @@ struct Bucket {
   uint32_t step_begin, step_end;  // stepwise steps
 };
 
-enum Topo : int32_t { kRing = 0, kMultiRing = 1, kTorus = 2 };
+enum Topo : int32_t { kRing = 0, kMultiRing = 1, kTorus = 2, kTorusND = 3 };
+constexpr int kMaxDims = 4;  // n-D torus: dims 0 (fastest in the rank number) .. 3
 enum Mode : int32_t { kFused = 0, kStepwise = 1, kRankOrder = 2 };
 
 struct Spec {
@@ -70,6 +71,7 @@ struct Spec {
   std::vector<uint64_t> layers;
   int mode = kFused;
   uint32_t tile_bytes = kTileBytes;  // bytes per rank in one work item
+  std::vector<int> dims;             // n-D torus sizes (trailing 1s dropped)
 };
 
 // Work-item size of the shared-memory-staged pass: P ranks' tiles of one

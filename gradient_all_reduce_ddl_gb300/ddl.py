@@ -38,7 +38,7 @@ EXPORTS = [
     "ddl_allreduce_bucket", "ddl_allreduce_host", "ddl_overlap_begin", "ddl_bucket_ready", "ddl_overlap_end",
     "ddl_plan_num_buckets", "ddl_plan_bucket_range", "ddl_plan_traffic", "ddl_plan_fold_order",
     "ddl_plan_launches", "ddl_plan_check", "ddl_status_string", "ddl_plan_destroy", "ddl_allreduce_noalloc",
-    "ddl_plan_cost",
+    "ddl_plan_cost", "ddl_plan_set_torus_dims",
 ]
 
 
@@ -60,6 +60,7 @@ def _sig(name, res, *args):
 _sig("ddl_plan_create", _i, _i, _sz, _i, ddl_topology_t, _sz, _P(_vp))
 _sig("ddl_plan_set_layers", _i, _vp, _i, _P(_sz))
 _sig("ddl_plan_set_mode", _i, _vp, _i)
+_sig("ddl_plan_set_torus_dims", _i, _vp, _i, _P(_i))
 _sig("ddl_plan_set_kernel", _i, _vp, _i)
 _sig("ddl_allreduce", _i, _vp, _P(_vp), _f, _vp)
 _sig("ddl_allreduce_bucket", _i, _vp, _i, _P(_vp), _f, _vp)
@@ -127,6 +128,11 @@ def ddl_plan_create(P, N, dtype, topology, bucket_bytes=0):
 def ddl_plan_set_layers(plan, numel_fwd_order):
     arr = (ctypes.c_size_t * len(numel_fwd_order))(*[int(v) for v in numel_fwd_order])
     _ok(_lib.ddl_plan_set_layers(plan, len(numel_fwd_order), arr), "ddl_plan_set_layers")
+
+
+def ddl_plan_set_torus_dims(plan, dims):
+    arr = (ctypes.c_int * len(dims))(*[int(d) for d in dims])
+    _ok(_lib.ddl_plan_set_torus_dims(plan, len(dims), arr), "ddl_plan_set_torus_dims")
 
 
 def ddl_plan_set_mode(plan, mode):
@@ -228,7 +234,7 @@ def ddl_allreduce_noalloc(P, N, dtype, topology, bucket_bytes, layers, rank_bufs
 
 # -- convenience object --------------------------------------------------------
 
-TOPOLOGIES = {"ring": DDL_RING, "multiring": DDL_MULTIRING, "torus": DDL_TORUS}
+TOPOLOGIES = {"ring": DDL_RING, "multiring": DDL_MULTIRING, "torus": DDL_TORUS, "torus_nd": DDL_RING}
 DTYPES = {"f32": DDL_FP32, "f16": DDL_FP16}
 MODES = {"fused": DDL_MODE_FUSED, "stepwise": DDL_MODE_STEPWISE, "rankorder": DDL_MODE_RANKORDER}
 KERNELS = {"auto": DDL_KERNEL_AUTO, "ldg": DDL_KERNEL_LDG, "bulk": DDL_KERNEL_BULK, "bulkload": DDL_KERNEL_BULK_LOAD}
@@ -238,13 +244,15 @@ class Plan:
     """An all-reduce plan for P rank buffers of N elements (owns a ddl_plan_t)."""
 
     def __init__(self, P, N, dtype="f32", topo="ring", k=1, X=0, Y=0, bucket_bytes=0, layers=None,
-                 mode="fused", kernel="auto"):
+                 mode="fused", kernel="auto", dims=None):
         self.P, self.N, self.dtype = int(P), int(N), dtype
         topo_t = ddl_topology_t(TOPOLOGIES[topo], int(k), int(X), int(Y))
         self.handle = ddl_plan_create(self.P, self.N, DTYPES[dtype], topo_t, int(bucket_bytes))
         try:
             if layers is not None:
                 ddl_plan_set_layers(self.handle, list(layers))
+            if topo == "torus_nd":
+                ddl_plan_set_torus_dims(self.handle, list(dims))
             if mode != "fused":
                 ddl_plan_set_mode(self.handle, MODES[mode])
             if kernel != "auto":
@@ -257,7 +265,7 @@ class Plan:
     @classmethod
     def for_workload(cls, w, **kw):
         return cls(w.P, w.N, w.dtype, w.topo, k=w.k, X=w.X, Y=w.Y, bucket_bytes=w.bucket_bytes,
-                   layers=w.layers, **kw)
+                   layers=w.layers, dims=getattr(w, "dims", None), **kw)
 
     def allreduce(self, rank_bufs, scale, stream=None):
         ddl_allreduce(self.handle, rank_bufs, scale, stream)

@@ -120,6 +120,20 @@ ddl_status_t ddl_plan_create(int P, size_t N, ddl_dtype_t dtype, ddl_topology_t 
  * bucket.  The array is copied.  Host-only. */
 ddl_status_t ddl_plan_set_layers(ddl_plan_t plan, int n_tensors, const size_t* numel_fwd_order);
 
+/* Makes the plan an n-dimensional torus: dims[0..ndims-1] (1 <= ndims <= 4,
+ * each >= 1, product == P), rank r at coordinates x_k = (r / (D_0...D_{k-1}))
+ * mod D_k (dim 0 varies fastest).  The schedule generalises the 2D-torus of
+ * "索尼发布新的方法，在ImageNet数据集上224秒内成功训练了ResNet-50"
+ * ("2D-Torus All-reduce", Fig. 1) to the several-level rings with which
+ * "[论文解读] PowerAI DDL" ("提出的方法") adapts to a machine's topology:
+ * reduce-scatter along dims 0..d-2, each line of D_k ranks working on the
+ * range it has reduced so far (a rank at x_k keeps part (x_k + 1) mod D_k),
+ * all-reduce along dim d-1 (scale applied at its owner), then all-gather
+ * along dims d-2..0.  Element results are d nested left folds, innermost over
+ * dim 0.  Trailing dims of size 1 are dropped; dims {X, Y} give exactly the
+ * DDL_TORUS result and dims {P} the ring's.  Host-only. */
+ddl_status_t ddl_plan_set_torus_dims(ddl_plan_t plan, int ndims, const int* dims);
+
 /* Selects the mode (default DDL_MODE_FUSED).  Host-only. */
 ddl_status_t ddl_plan_set_mode(ddl_plan_t plan, ddl_mode_t mode);
 

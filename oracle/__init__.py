@@ -33,7 +33,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-TOPO = {"ring": 0, "multiring": 1, "torus": 2}
+TOPO = {"ring": 0, "multiring": 1, "torus": 2, "torus_nd": 3}
 DTYPE = {"f32": 0, "f16": 1}
 
 
@@ -60,6 +60,8 @@ class _Cfg(ctypes.Structure):
         ("bucket_bytes", ctypes.c_uint64),
         ("n_layers", ctypes.c_int64),
         ("layers", ctypes.POINTER(ctypes.c_uint64)),
+        ("ndims", ctypes.c_int32),
+        ("dims", ctypes.c_int32 * 4),
     ]
 
 
@@ -100,7 +102,7 @@ class Config:
     """One all-reduce problem: P rank buffers of N elements, a schedule and buckets."""
 
     def __init__(self, P: int, N: int, dtype: str = "f32", topo: str = "ring", k: int = 1,
-                 X: int = 0, Y: int = 0, bucket_bytes: int = 0, layers=None):
+                 X: int = 0, Y: int = 0, bucket_bytes: int = 0, layers=None, dims=None):
         self.P, self.N, self.dtype, self.topo = int(P), int(N), dtype, topo
         self.k, self.X, self.Y, self.bucket_bytes = int(k), int(X), int(Y), int(bucket_bytes)
         self._layers = None if layers is None else np.ascontiguousarray(layers, dtype=np.uint64)
@@ -112,6 +114,11 @@ class Config:
             c.layers = self._layers.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64))
         else:
             c.n_layers = 0
+        self.dims = None if dims is None else [int(d) for d in dims]
+        if self.dims is not None:
+            c.ndims = len(self.dims)
+            for i, d in enumerate(self.dims[:4]):
+                c.dims[i] = d
         self._c = c
 
     @property

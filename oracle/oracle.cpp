@@ -119,7 +119,8 @@ uint16_t float_to_half(float v) {
 /* ------------------------------------------------------------------------ */
 
 enum { DT_F32 = 0, DT_F16 = 1 };
-enum { TOPO_RING = 0, TOPO_MULTIRING = 1, TOPO_TORUS = 2 };
+enum { TOPO_RING = 0, TOPO_MULTIRING = 1, TOPO_TORUS = 2, TOPO_TORUS_ND = 3 };
+constexpr int MAX_DIMS = 4;
 
 struct Cfg {
   int P;
@@ -130,6 +131,7 @@ struct Cfg {
   int X, Y;
   uint64_t bucket_bytes;
   std::vector<uint64_t> layers; /* numel per tensor, forward order; may be empty */
+  std::vector<int> dims;        /* n-D torus: sizes of dims 0 (fastest) .. d-1 */
   uint64_t esize() const { return dtype == DT_F16 ? 2 : 4; }
 };
 
@@ -160,6 +162,11 @@ int validate(const Cfg& c) {
     if (c.k < 1 || !ring_strides(c.P, c.k, s)) return -3;
   } else if (c.topo == TOPO_TORUS) {
     if (c.X < 1 || c.Y < 1 || (int64_t)c.X * c.Y != c.P) return -4;
+  } else if (c.topo == TOPO_TORUS_ND) {
+    if (c.dims.empty() || (int)c.dims.size() > MAX_DIMS) return -4;
+    int64_t prod = 1;
+    for (int d : c.dims) { if (d < 1) return -4; prod *= d; }
+    if (prod != c.P) return -4;
   } else if (c.topo != TOPO_RING) {
     return -5;
   }
@@ -382,11 +389,85 @@ struct Emu {
     }
   }
 
+  /* n-D torus, rank r = x0 + D0*(x1 + D1*(x2 + ...)).  Phase k < d-1:
+   * reduce-scatter along dim k, every line of D_k ranks (other coordinates
+   * fixed) on the range that line already reduced; the last dim all-reduces
+   * its range (the owner's last add is final); then all-gathers along dims
+   * d-2 .. 0.  The range a rank holds after the reduce-scatters along dims
+   * 0..k-1 is: start from the bucket, take part (x_j + 1 mod D_j) of D_j
+   * parts for j = 0..k-1 (its reduce-scatter ends at position c - 1). */
+  void range_of(const std::vector<int>& x, int k, uint64_t lo, uint64_t hi, uint64_t* a, uint64_t* b) const {
+    uint64_t s0 = lo, n = hi - lo;
+    for (int j = 0; j < k; ++j) {
+      const int D = c.dims[j];
+      const uint64_t part = (uint64_t)((x[j] + 1) % D);
+      s0 += part_start(n, D, part);
+      n = part_size(n, D, part);
+    }
+    *a = s0;
+    *b = s0 + n;
+  }
+  void coords(int r, std::vector<int>& x) const {
+    x.assign(c.dims.size(), 0);
+    for (size_t j = 0; j < c.dims.size(); ++j) { x[j] = r % c.dims[j]; r /= c.dims[j]; }
+  }
+  int rank_of(const std::vector<int>& x) const {
+    int r = 0;
+    for (size_t j = c.dims.size(); j-- > 0;) r = r * c.dims[j] + x[j];
+    return r;
+  }
+  /* every line along dim k: the ranks in ring order (position = x_k) */
+  std::vector<std::vector<int>> lines(int k) const {
+    std::vector<std::vector<int>> out;
+    std::vector<int> x;
+    for (int r = 0; r < c.P; ++r) {
+      coords(r, x);
+      if (x[k] != 0) continue;
+      std::vector<int> ring(c.dims[k]);
+      for (int t = 0; t < c.dims[k]; ++t) { x[k] = t; ring[t] = rank_of(x); }
+      out.push_back(ring);
+    }
+    return out;
+  }
+  void torus_nd_bucket(uint64_t lo, uint64_t hi) {
+    const int d = (int)c.dims.size();
+    std::vector<int> x;
+    for (int k = 0; k < d; ++k) {
+      const bool last_dim = (k == d - 1);
+      const auto L = lines(k);
+      for (int s = 0; s + 1 < c.dims[k]; ++s) {
+        for (const auto& ring : L) {
+          coords(ring[0], x);
+          uint64_t a, b;
+          range_of(x, k, lo, hi, &a, &b);
+          rs_send(ring, a, b, s, last_dim);
+        }
+        step();
+      }
+      /* a ring of one at the last dim: the owner scales (only when P = 1,
+       * since trailing dims of size 1 are dropped when the config is loaded) */
+      if (last_dim && c.dims[k] == 1) owner_scale_only(0, lo, hi);
+    }
+    for (int k = d - 1; k >= 0; --k) {
+      const auto L = lines(k);
+      for (int s = 0; s + 1 < c.dims[k]; ++s) {
+        for (const auto& ring : L) {
+          coords(ring[0], x);
+          uint64_t a, b;
+          range_of(x, k, lo, hi, &a, &b);
+          ag_send(ring, a, b, s);
+        }
+        step();
+      }
+    }
+  }
+
   void run() {
     for (const auto& bk : make_buckets(c)) {
       if (c.topo == TOPO_RING) ring_bucket(bk.first, bk.second);
       else if (c.topo == TOPO_MULTIRING) multiring_bucket(bk.first, bk.second);
-      else torus_bucket(bk.first, bk.second);
+      else if (c.topo == TOPO_TORUS) torus_bucket(bk.first, bk.second);
+      else torus_nd_bucket(bk.first, bk.second);
     }
   }
 };
@@ -397,7 +478,7 @@ struct Emu {
 /* the multi-ring as a single group of P.                                   */
 /* ------------------------------------------------------------------------ */
 
-struct Order { std::vector<int> rank; int inner, groups; };
+struct Order { std::vector<int> rank; int inner, groups; std::vector<int> lev; /* n-D: level sizes */ };
 
 Order fold_order(const Cfg& c, const std::vector<std::pair<uint64_t, uint64_t>>& bk, uint64_t i) {
   Order o;
@@ -417,15 +498,58 @@ Order fold_order(const Cfg& c, const std::vector<std::pair<uint64_t, uint64_t>>&
     const int ch = (int)part_of(nj, c.P, off - a);
     for (int t = 0; t < c.P; ++t) o.rank[t] = (int)(((int64_t)((ch + t) % c.P) * sj[j]) % c.P);
     o.inner = c.P; o.groups = 1;
-  } else {
+  } else if (c.topo == TOPO_TORUS) {
     const int ch = (int)part_of(n, c.X, off);
     const uint64_t a = part_start(n, c.X, ch), nc = part_size(n, c.X, ch);
     const int d = (int)part_of(nc, c.Y, off - a);
     for (int g = 0; g < c.Y; ++g)
       for (int h = 0; h < c.X; ++h) o.rank[g * c.X + h] = ((d + g) % c.Y) * c.X + (ch + h) % c.X;
     o.inner = c.X; o.groups = c.Y;
+  } else {
+    /* n-D torus: the chunk index along every dim, then the nested order:
+     * position (g_0 + D0*(g_1 + D1*...)) holds the rank with coordinates
+     * x_k = (c_k + g_k) mod D_k */
+    const int d = (int)c.dims.size();
+    std::vector<int> ch(d);
+    uint64_t a = 0, m = n;
+    for (int k = 0; k < d; ++k) {
+      ch[k] = (int)part_of(m, c.dims[k], off - a);
+      a += part_start(m, c.dims[k], ch[k]);
+      m = part_size(m, c.dims[k], ch[k]);
+    }
+    for (int t = 0; t < c.P; ++t) {
+      int rest = t, r = 0, stride = 1;
+      for (int k = 0; k < d; ++k) {
+        const int g = rest % c.dims[k];
+        rest /= c.dims[k];
+        r += ((ch[k] + g) % c.dims[k]) * stride;
+        stride *= c.dims[k];
+      }
+      o.rank[t] = r;
+    }
+    o.lev = c.dims;
+    o.inner = c.dims[0]; o.groups = c.P / c.dims[0];
   }
   return o;
+}
+
+float hop_add(float a, float b, bool last, int dtype);
+
+/* Nested left fold: a group at level l is the left fold of its lev[l]
+ * subgroups at level l-1 (level -1 = one rank's value).  Every add is rounded
+ * to the storage type (R6) except the very last one, which is the add of the
+ * last subgroup at the highest level of size > 1. */
+float fold_group(const Order& o, const float* x, int l, int base, int top, int dtype) {
+  if (l < 0) return x[o.rank[base]];
+  int sub = 1;
+  for (int j = 0; j < l; ++j) sub *= o.lev[j];
+  float acc = fold_group(o, x, l - 1, base, top, dtype);
+  for (int m = 1; m < o.lev[l]; ++m) {
+    const float v = fold_group(o, x, l - 1, base + m * sub, top, dtype);
+    const bool last = (l == top && m == o.lev[l] - 1);
+    acc = hop_add(acc, v, last, dtype);
+  }
+  return acc;
 }
 
 /* R6: a result that travels again is rounded to the storage type. */
@@ -437,6 +561,14 @@ float hop_add(float a, float b, bool last, int dtype) {
 
 /* x[r] = binary32 value of rank r's element; returns the stored result bits. */
 uint32_t closed_form_value(const Cfg& c, const Order& o, const float* x, float scale) {
+  if (!o.lev.empty()) {
+    int top = -1;
+    for (int l = 0; l < (int)o.lev.size(); ++l)
+      if (o.lev[l] > 1) top = l;
+    const float v = fold_group(o, x, (int)o.lev.size() - 1, 0, top, c.dtype);
+    const float r = v * scale;
+    return c.dtype == DT_F16 ? (uint32_t)float_to_half(r) : f32_bits(r);
+  }
   float outer = 0.0f;
   for (int g = 0; g < o.groups; ++g) {
     float inner = x[o.rank[g * o.inner]];
@@ -469,6 +601,8 @@ typedef struct {
   uint64_t bucket_bytes;
   int64_t n_layers;
   const uint64_t* layers;
+  int32_t ndims;     /* n-D torus (topo 3): number of dims, 1..4 */
+  int32_t dims[4];   /* sizes, dim 0 varies fastest in the rank number */
 } oracle_cfg;
 
 static int load_cfg(const oracle_cfg* in, Cfg& c) {
@@ -477,6 +611,14 @@ static int load_cfg(const oracle_cfg* in, Cfg& c) {
   c.k = in->k; c.X = in->X; c.Y = in->Y; c.bucket_bytes = in->bucket_bytes;
   c.layers.clear();
   if (in->n_layers > 0 && in->layers) c.layers.assign(in->layers, in->layers + in->n_layers);
+  c.dims.clear();
+  if (c.topo == TOPO_TORUS_ND) {
+    if (in->ndims < 1 || in->ndims > MAX_DIMS) return -4;
+    c.dims.assign(in->dims, in->dims + in->ndims);
+    /* trailing dims of size 1 add no step; drop them so that the last
+     * remaining dim carries the all-reduce with the final add */
+    while (c.dims.size() > 1 && c.dims.back() == 1) c.dims.pop_back();
+  }
   return validate(c);
 }
 

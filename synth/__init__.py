@@ -122,12 +122,13 @@ class Workload:
     P: int
     N: int
     dtype: str            # "f32" or "f16"
-    topo: str             # "ring" | "multiring" | "torus"
+    topo: str             # "ring" | "multiring" | "torus" | "torus_nd"
     k: int = 1
     X: int = 0
     Y: int = 0
     bucket_bytes: int = 0
     layers: tuple | None = None
+    dims: tuple | None = None   # n-D torus sizes (topo "torus_nd")
     scale: float = 1.0
     dist: str = "normal"
     sigma: float = 1.0
@@ -169,6 +170,10 @@ WORKLOADS = {
                                       topo="multiring", k=4, bucket_bytes=25 * 2 ** 20,
                                       layers=tuple(RESNET101), scale=1.0 / 64, sigma=1e-3,
                                       seed=_SEED0 + 4),
+    # n-D torus 4x4x4 (P=64) on the ResNet-101 gradient in 25 MiB buckets
+    "torus4x4x4_resnet101": Workload("torus4x4x4_resnet101", P=64, N=sum(RESNET101), dtype="f32",
+                                     topo="torus_nd", dims=(4, 4, 4), bucket_bytes=25 * 2 ** 20,
+                                     layers=tuple(RESNET101), scale=1.0 / 64, sigma=1e-3, seed=_SEED0 + 6),
     # P=16, 300M fp32 (1.2 GB per rank, the language model's gradient), N(0, 1e-4)
     "ring16_lm300m": Workload("ring16_lm300m", P=16, N=300_000_000, dtype="f32", topo="ring",
                               scale=1.0 / 16, sigma=1e-4, seed=_SEED0 + 5),

@@ -43,7 +43,7 @@ def device_bufs_generated(w, device, pad_elems=0):
 
 def oracle_cfg(w):
     return oracle.Config(w.P, w.N, w.dtype, w.topo, k=w.k, X=w.X, Y=w.Y, bucket_bytes=w.bucket_bytes,
-                         layers=w.layers)
+                         layers=w.layers, dims=w.dims)
 
 
 def part_edges(lo, hi, m):
@@ -62,6 +62,15 @@ def edge_samples(w):
         if w.topo == "torus":
             for c0, c1 in zip(part_edges(lo, hi, w.X)[:-1], part_edges(lo, hi, w.X)[1:]):
                 edges.update(part_edges(c0, c1, w.Y))
+        elif w.topo == "torus_nd":
+            level = [(lo, hi)]
+            for D in w.dims:
+                nxt = []
+                for a, b in level:
+                    e = part_edges(a, b, D)
+                    edges.update(e)
+                    nxt += list(zip(e[:-1], e[1:]))
+                level = nxt
         elif w.topo == "multiring":
             for s0, s1 in zip(part_edges(lo, hi, w.k)[:-1], part_edges(lo, hi, w.k)[1:]):
                 edges.update(part_edges(s0, s1, w.P))

@@ -43,10 +43,11 @@ def test_status_strings(ddl):
     assert "unknown" in ddl.ddl_status_string(99)
 
 
-def _pair(P, N, dtype="f32", topo="ring", k=1, X=0, Y=0, bucket_bytes=0, layers=None, mode="fused"):
+def _pair(P, N, dtype="f32", topo="ring", k=1, X=0, Y=0, bucket_bytes=0, layers=None, mode="fused", dims=None):
     from gradient_all_reduce_ddl_gb300 import ddl
-    plan = ddl.Plan(P, N, dtype, topo, k=k, X=X, Y=Y, bucket_bytes=bucket_bytes, layers=layers, mode=mode)
-    cfg = oracle.Config(P, N, dtype, topo, k=k, X=X, Y=Y, bucket_bytes=bucket_bytes, layers=layers)
+    plan = ddl.Plan(P, N, dtype, topo, k=k, X=X, Y=Y, bucket_bytes=bucket_bytes, layers=layers, mode=mode,
+                    dims=dims)
+    cfg = oracle.Config(P, N, dtype, topo, k=k, X=X, Y=Y, bucket_bytes=bucket_bytes, layers=layers, dims=dims)
     return plan, cfg
 
 
@@ -62,6 +63,10 @@ CASES = [
     dict(P=12, N=500, topo="torus", X=3, Y=4),
     dict(P=6, N=50, topo="torus", X=6, Y=1, dtype="f16", bucket_bytes=30),
     dict(P=6, N=50, topo="torus", X=1, Y=6, layers=[10, 20, 15, 5], bucket_bytes=40),
+    dict(P=8, N=77, topo="torus_nd", dims=[2, 2, 2]),
+    dict(P=64, N=1001, topo="torus_nd", dims=[4, 4, 4], bucket_bytes=1200),
+    dict(P=24, N=333, topo="torus_nd", dims=[2, 3, 2, 2], dtype="f16"),
+    dict(P=12, N=120, topo="torus_nd", dims=[3, 1, 4, 1]),
 ]
 
 
@@ -117,6 +122,16 @@ def test_staged_kernel_tables_match_oracle(ddl, case):
         for i in range(cfg.N):
             o_ord, o_in, o_gr = oracle.fold_order(cfg, i)
             assert plan.fold_order(i) == (o_ord.tolist(), o_in, o_gr), i
+
+
+def test_nd_torus_dims_validation(ddl):
+    E = ddl.DDLError
+    with ddl.Plan(8, 100) as p:
+        for dims in ([3, 3], [0, 8], [2, 2, 2, 1, 1], []):
+            with pytest.raises(E):
+                ddl.ddl_plan_set_torus_dims(p.handle, dims)
+        ddl.ddl_plan_set_torus_dims(p.handle, [2, 4, 1])     # trailing 1 dropped
+        assert p.traffic() == oracle.traffic(oracle.Config(8, 100, topo="torus", X=2, Y=4))
 
 
 def test_rankorder_and_stepwise_tables(ddl):

@@ -30,14 +30,14 @@ DEV = "cuda:0"
 
 
 def _w(P, N, dtype="f32", topo="ring", k=1, X=0, Y=0, bucket_bytes=0, layers=None, dist="normal", sigma=None,
-       scale=None, seed=1):
+       scale=None, seed=1, dims=None):
     if sigma is None:
         sigma = 1e-2 if dtype == "f16" else 1e-3
     if scale is None:
         scale = float(np.float32(1.0 / P))
     return synth.Workload(name="t", P=P, N=N, dtype=dtype, topo=topo, k=k, X=X, Y=Y, bucket_bytes=bucket_bytes,
                           layers=None if layers is None else tuple(layers), scale=scale, dist=dist, sigma=sigma,
-                          seed=seed)
+                          seed=seed, dims=None if dims is None else tuple(dims))
 
 
 def _host_inputs(w):
@@ -89,6 +89,10 @@ SMALL = [
     dict(P=6, N=12_345, topo="torus", X=1, Y=6),
     dict(P=200, N=3001, topo="ring"),
     dict(P=16, N=20_000, layers=[1000, 5000, 3, 7000, 6997], bucket_bytes=20_000),
+    dict(P=8, N=30_001, topo="torus_nd", dims=[2, 2, 2]),
+    dict(P=64, N=20_011, topo="torus_nd", dims=[4, 4, 4], bucket_bytes=30_000),
+    dict(P=24, N=17_777, topo="torus_nd", dims=[2, 3, 2, 2]),
+    dict(P=12, N=9_001, topo="torus_nd", dims=[3, 1, 4]),
 ]
 
 
@@ -103,14 +107,15 @@ def test_fused_matches_oracle(ddl, case, dtype, kernel):
 
 @pytest.mark.parametrize("kernel", ["ldg", "bulk"])
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
-@pytest.mark.parametrize("case", [SMALL[4], SMALL[7], SMALL[11], SMALL[16]])
+@pytest.mark.parametrize("case", [SMALL[4], SMALL[7], SMALL[11], SMALL[16], SMALL[18]])
 def test_fused_unaligned_buffers_match_oracle(ddl, case, dtype, kernel):
     """Rank pointers that are not 16-byte aligned take the element-wise path."""
     _check_exact(ddl, _w(dtype=dtype, **case), misalign=1, kernel=kernel)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
-@pytest.mark.parametrize("case", [SMALL[0], SMALL[1], SMALL[4], SMALL[7], SMALL[10], SMALL[12], SMALL[14]])
+@pytest.mark.parametrize("case", [SMALL[0], SMALL[1], SMALL[4], SMALL[7], SMALL[10], SMALL[12], SMALL[14],
+                                  SMALL[17], SMALL[19]])
 def test_stepwise_matches_oracle(ddl, case, dtype):
     if dtype == "f16" and case.get("dist") == "int1000":
         pytest.skip("integer case is fp32")
@@ -152,7 +157,7 @@ def test_device_generator_matches_host(ddl):
 # ---------------------------------------------------------------------------
 
 FULL = ["ring4_int", "torus4x4_resnet50", "torus8x4_resnet50_f16", "multiring64_resnet101", "ring16_lm300m",
-        "multiring16_lm300m", "torus4x4_lm300m"]
+        "multiring16_lm300m", "torus4x4_lm300m", "torus4x4x4_resnet101"]
 
 
 @pytest.mark.parametrize("kernel", ["auto", "bulk", "bulkload"])

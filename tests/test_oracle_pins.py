@@ -454,3 +454,104 @@ def test_generator_statistics_and_counter_access():
     assert h.dtype == np.uint16
     # SplitMix64 published first output for seed 0 (state 0 + gamma)
     assert int(synth._mix(np.array([0x9E3779B97F4A7C15], dtype=np.uint64))[0]) == 0xE220A8397B1DCDAF
+
+
+# --------------------------------------------------------------------------
+# n-D torus (generalising the 2D torus of the Sony page's "2D-Torus
+# All-reduce" to the multi-level rings of "[论文解读] PowerAI DDL")
+# --------------------------------------------------------------------------
+
+ND_CASES = [
+    dict(P=8, N=77, dims=[2, 2, 2]),
+    dict(P=12, N=500, dims=[2, 3, 2], bucket_bytes=600),
+    dict(P=64, N=1001, dims=[4, 4, 4]),
+    dict(P=24, N=333, dims=[2, 3, 2, 2]),
+    dict(P=16, N=100, dims=[4, 1, 4]),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("dims,other", [([4, 4], dict(topo="torus", X=4, Y=4)), ([16], dict(topo="ring")),
+                                        ([3, 4, 1], dict(topo="torus", X=3, Y=4)), ([1, 12], dict(topo="ring")),
+                                        ([12, 1, 1], dict(topo="ring")), ([4, 1, 3], dict(topo="torus", X=4, Y=3))])
+def test_nd_torus_reduces_to_torus_and_ring(oracle_lib, dtype, dims, other):
+    P = int(np.prod(dims))
+    rng = np.random.default_rng(P * 7 + len(dims))
+    for bucket_bytes in (0, 300):
+        ins = _wide_random(rng, P, 257, dtype)
+        a = [b.copy() for b in ins]
+        b = [b.copy() for b in ins]
+        ma = oracle.emulate(oracle.Config(P=P, N=257, dtype=dtype, topo="torus_nd", dims=dims,
+                                          bucket_bytes=bucket_bytes), a, 1 / P)
+        mb = oracle.emulate(oracle.Config(P=P, N=257, dtype=dtype, bucket_bytes=bucket_bytes, **other), b, 1 / P)
+        assert ma == mb
+        assert all(np.array_equal(a[r], b[r]) for r in range(P))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("case", ND_CASES)
+def test_nd_torus_emulation_equals_closed_form(oracle_lib, case, dtype):
+    rng = np.random.default_rng(zlib.crc32(repr((sorted(case.items()), dtype)).encode()))
+    cfg = oracle.Config(dtype=dtype, topo="torus_nd", **case)
+    ins = _wide_random(rng, cfg.P, cfg.N, dtype)
+    bufs = [b.copy() for b in ins]
+    oracle.emulate(cfg, bufs, 1 / cfg.P)
+    for r in range(1, cfg.P):
+        assert np.array_equal(bufs[r], bufs[0])
+    assert np.array_equal(oracle.closed_form_full(cfg, ins, 1 / cfg.P), bufs[0])
+
+
+@pytest.mark.parametrize("case", ND_CASES)
+def test_nd_torus_exact_sums_traffic_steps(oracle_lib, case):
+    rng = np.random.default_rng(3)
+    cfg = oracle.Config(topo="torus_nd", **case)
+    ints = rng.integers(-1000, 1001, size=(cfg.P, cfg.N))
+    bufs = [ints[r].astype(np.float32) for r in range(cfg.P)]
+    moved, steps = oracle.emulate(cfg, bufs, 1.0)
+    for r in range(cfg.P):
+        assert np.array_equal(bufs[r], ints.sum(axis=0).astype(np.float32))
+    nb = len(oracle.buckets(cfg))
+    assert moved == 2 * (cfg.P - 1) * cfg.N
+    assert steps == nb * sum(2 * (d - 1) for d in case["dims"])
+
+
+@pytest.mark.parametrize("dims", [[2, 2], [2, 1, 2], [1, 2, 2], [2, 2, 1], [4], [1, 1, 1, 3]])
+def test_nd_torus_brute_force_one_hot(oracle_lib, dims):
+    P = int(np.prod(dims))
+    for dtype in ("f32", "f16"):
+        one = np.float16(1).view(np.uint16) if dtype == "f16" else np.float32(1)
+        half = np.float16(0.5).view(np.uint16) if dtype == "f16" else np.float32(0.5)
+        npdt = np.uint16 if dtype == "f16" else np.float32
+        for N in (1, 3, 7):
+            for src, i in itertools.product(range(P), range(N)):
+                cfg = oracle.Config(P=P, N=N, dtype=dtype, topo="torus_nd", dims=dims)
+                bufs = [np.zeros(N, dtype=npdt) for _ in range(P)]
+                bufs[src][i] = one
+                oracle.emulate(cfg, bufs, 0.5)
+                expect = np.zeros(N, dtype=npdt)
+                expect[i] = half
+                assert all(np.array_equal(b, expect) for b in bufs), (dims, dtype, N, src, i)
+
+
+def test_nd_torus_2x2x2_fold_order_by_hand(oracle_lib):
+    """2x2x2 cube, N=8: each element is its own chunk tuple.  Element 5 has
+    chunks (c0, c1, c2) = (1, 0, 1) (halves of 8, then of 4, then of 2).  Its
+    fold visits x_k = (c_k + g_k) mod 2, g_0 fastest, rank = x0 + 2 x1 + 4 x2:
+    ranks 5, 4, 7, 6, 1, 0, 3, 2, grouped ((5+4)+(7+6)) + ((1+0)+(3+2))."""
+    cfg = oracle.Config(P=8, N=8, topo="torus_nd", dims=[2, 2, 2])
+    assert oracle.fold_order(cfg, 5)[0].tolist() == [5, 4, 7, 6, 1, 0, 3, 2]
+    assert oracle.fold_order(cfg, 0)[0].tolist() == [0, 1, 2, 3, 4, 5, 6, 7]
+    # E = 2^24: nested groups give (E+1 -> E) + (1+1) = E+2, then + 0; a flat
+    # left fold over the same order would give ((E+1)+1)+1 -> E
+    E = 16777216.0
+    vals = np.zeros((8, 8), dtype=np.float32)
+    vals[5, 5], vals[4, 5], vals[7, 5], vals[6, 5] = E, 1, 1, 1
+    bufs = [vals[r].copy() for r in range(8)]
+    oracle.emulate(cfg, bufs, 1.0)
+    assert bufs[0][5] == E + 2 and bufs[3][5] == E + 2
+
+
+def test_nd_torus_invalid_dims(oracle_lib):
+    for dims in ([3, 3], [0, 8], [2, 2, 2, 1, 1]):
+        with pytest.raises(oracle.OracleError):
+            oracle.traffic(oracle.Config(P=8, N=10, topo="torus_nd", dims=dims))
