@@ -250,6 +250,49 @@ def overlap_study(plan, bufs, w, stream, steps: int = 20, tokens: int = 2048):
     return out
 
 
+def sgd_study(plan, bufs, w, stream, steps: int = 50):
+    """All-reduce + momentum-SGD update: the fused pass (ddl_allreduce_sgd)
+    against the all-reduce followed by an unfused update of the P replicas'
+    parameters (torch foreach kernels)."""
+    import torch
+    dev = bufs[0].device
+    params = [torch.zeros(w.N, device=dev) for _ in range(w.P)]
+    moms = [torch.zeros(w.N, device=dev) for _ in range(w.P)]
+    lr, mu, wd = 0.01, 0.9, 1e-4
+
+    def fused():
+        plan.allreduce_sgd(bufs, params, moms, w.scale, lr, mu, wd, keep_grads=True, stream=stream)
+
+    def unfused():
+        plan.allreduce(bufs, w.scale, stream)
+        g = [b.float() for b in bufs] if w.dtype == "f16" else bufs
+        d = torch._foreach_add(g, params, alpha=wd)
+        torch._foreach_mul_(moms, mu)
+        torch._foreach_add_(moms, d)
+        torch._foreach_add_(params, moms, alpha=-lr)
+
+    out = {}
+    with torch.cuda.stream(stream):
+        for name, fn in [("fused", fused), ("unfused", unfused)]:
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize(dev)
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(steps):
+                fn()
+            s1.record(stream)
+            torch.cuda.synchronize(dev)
+            out[name + "_ms"] = round(s0.elapsed_time(s1) / steps, 4)
+    algo = w.P * w.N * (2 * w.esize + 16)  # gradient read + write, parameter and momentum read + write
+    out["fused_bytes_per_step"] = algo
+    out["fused_GBps"] = round(algo / (out["fused_ms"] * 1e-3) / 1e9, 1)
+    out["fused_frac_of_hbm"] = round(out["fused_GBps"] / measured_peak()[0], 4)
+    out["update"] = "d = g + wd p; v = mu v + d; p = p - lr v on every rank's fp32 copy (lr 0.01, mu 0.9, wd 1e-4)"
+    del params, moms
+    return out
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -306,6 +349,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--overlap", action="store_true",
                     help="also time a synthetic backward overlapped with the bucketed all-reduce")
+    ap.add_argument("--sgd", action="store_true",
+                    help="also time the all-reduce fused with the momentum-SGD update")
     ap.add_argument("--overlap-tokens", type=int, default=2048,
                     help="GEMM rows of the synthetic backward (its compute per parameter)")
     ap.add_argument("--graph", action="store_true",
@@ -454,6 +499,8 @@ def main():
         overlap = overlap_study(plan, bufs, w, stream, tokens=args.overlap_tokens)
         overlap["allreduce_alone_ms"] = round(ms_per_step, 4)
 
+    sgd = sgd_study(plan, bufs, w, stream) if args.sgd else None
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = cpu_baseline(w)
@@ -475,7 +522,7 @@ def main():
                            "l2": f"inputs {w.P * w.N * w.esize / 1e9:.2f} GB per replica, larger than the 129 MB L2",
                            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU, P logical ranks"},
                 "clocks": clk, "gpu_launches": launches, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
-                "cluster_model": model, "overlap": overlap,
+                "cluster_model": model, "overlap": overlap, "sgd": sgd,
                 "kernel_src": kernel_hash()}
         print(json.dumps(line), flush=True)
     plan.close()

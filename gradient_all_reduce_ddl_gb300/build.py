@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "libddl.so")
 BUILD = os.path.join(ROOT, "_build", "ddl")
 
-SOURCES = ["plan.cpp", "ddl_api.cu", "fold_kernels.cu", "step_kernels.cu", "noalloc.cu"]
+SOURCES = ["plan.cpp", "ddl_api.cu", "fold_kernels.cu", "step_kernels.cu", "noalloc.cu", "sgd_kernels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC,-Wall",
          "-I", INCLUDE, "-I", CSRC]

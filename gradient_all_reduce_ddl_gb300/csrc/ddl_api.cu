@@ -40,6 +40,9 @@ struct ddl_plan {
   // last rank-pointer set that passed the device-pointer check
   std::vector<void*> checked;
   bool checked_aligned = false;
+  // last parameter / momentum pointer set that passed the checks
+  std::vector<void*> checked_sgd;
+  bool checked_sgd_aligned = false;
   // host-buffer pipeline: copy-in, compute and copy-out streams, events
   cudaStream_t hs[3] = {nullptr, nullptr, nullptr};
   std::vector<cudaEvent_t> hev;
@@ -391,6 +394,75 @@ ddl_status_t ddl_allreduce(ddl_plan_t p, void* const* bufs, float scale, void* s
   for (int b = 0; b < (int)p->tab.buckets.size(); ++b) {
     st = run_bucket(p, b, bufs, aligned, scale, static_cast<cudaStream_t>(stream));
     if (st != DDL_OK) return st;
+  }
+  return DDL_OK;
+}
+
+ddl_status_t ddl_allreduce_sgd(ddl_plan_t p, void* const* grad_bufs, float* const* param_bufs, float* const* mom_bufs,
+                               float scale, float lr, float momentum, float weight_decay, int keep_grads,
+                               void* stream) {
+  if (!p || !param_bufs) return DDL_ERR_INVALID_ARG;
+  if (p->spec.mode == ddl::kStepwise || p->spec.topo == ddl::kTorusND || p->spec.P > ddl::kMaxPSgd)
+    return DDL_ERR_UNSUPPORTED;
+  if (!mom_bufs && momentum != 0.0f) return DDL_ERR_INVALID_ARG;
+  if (p->ov_active) return DDL_ERR_INVALID_ARG;
+  const int P = p->spec.P;
+  bool aligned = false;
+  ddl_status_t st = prepare(p, grad_bufs, &aligned);
+  if (st != DDL_OK) return st;
+  // parameters and momenta: distinct, non-overlapping binary32 device arrays
+  std::vector<void*> cur(param_bufs, param_bufs + P);
+  if (mom_bufs) cur.insert(cur.end(), mom_bufs, mom_bufs + P);
+  if (p->checked_sgd != cur) {
+    const uint64_t gbytes = p->spec.N * (uint64_t)p->spec.esize, fbytes = p->spec.N * 4ull;
+    std::vector<std::pair<uintptr_t, uint64_t>> all;
+    for (int r = 0; r < P; ++r) all.push_back({reinterpret_cast<uintptr_t>(grad_bufs[r]), gbytes});
+    bool al = true;
+    for (void* q : cur) {
+      if (!q) return DDL_ERR_INVALID_ARG;
+      all.push_back({reinterpret_cast<uintptr_t>(q), fbytes});
+      al = al && (reinterpret_cast<uintptr_t>(q) % 16 == 0);
+      cudaPointerAttributes at;
+      if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+        cudaGetLastError();
+        return DDL_ERR_INVALID_ARG;
+      }
+      if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return DDL_ERR_INVALID_ARG;
+    }
+    std::sort(all.begin(), all.end());
+    for (size_t i = 0; i + 1 < all.size(); ++i)
+      if (all[i].first + all[i].second > all[i + 1].first) return DDL_ERR_INVALID_ARG;
+    p->checked_sgd = cur;
+    p->checked_sgd_aligned = al;
+  }
+  ddl::SgdParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  sp.items = p->d_items;
+  sp.segs = p->d_segs;
+  sp.orders = p->d_orders;
+  sp.err = p->d_err;
+  sp.n_segs = (uint32_t)p->tab.segs.size();
+  sp.n_orders = (uint32_t)p->tab.orders.size();
+  sp.P = P;
+  sp.scale = scale;
+  sp.lr = lr;
+  sp.mu = momentum;
+  sp.wd = weight_decay;
+  sp.round_hops = (p->spec.esize == 2 && p->spec.mode == ddl::kFused) ? 1 : 0;
+  sp.vector_ok = (aligned && p->checked_sgd_aligned) ? 1 : 0;
+  sp.keep_grads = keep_grads ? 1 : 0;
+  sp.has_mom = mom_bufs ? 1 : 0;
+  for (int r = 0; r < P; ++r) {
+    sp.grads[r] = grad_bufs[r];
+    sp.params[r] = param_bufs[r];
+    sp.moms[r] = mom_bufs ? mom_bufs[r] : nullptr;
+  }
+  for (const ddl::Bucket& bk : p->tab.buckets) {
+    sp.item0 = bk.item_begin;
+    const cudaError_t e =
+        ddl::launch_sgd(sp, bk.item_end - bk.item_begin, p->spec.esize == 2, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
+    ++p->launches;
   }
   return DDL_OK;
 }

@@ -38,6 +38,29 @@ struct FoldParams {
   void* bufs[kMaxP];   // rank r's buffer
 };
 
+// Fused all-reduce + momentum SGD (rank pointers of three buffer sets).
+constexpr int kMaxPSgd = 128;
+struct SgdParams {
+  const Item* items;
+  const Segment* segs;
+  const uint8_t* orders;
+  uint32_t* err;
+  uint32_t item0;
+  uint32_t n_segs;
+  uint32_t n_orders;
+  int32_t P;
+  float scale, lr, mu, wd;
+  int32_t round_hops;
+  int32_t vector_ok;   // every buffer 16-byte aligned
+  int32_t keep_grads;  // store the all-reduced gradient back
+  int32_t has_mom;     // momentum buffers given (else v = d)
+  void* grads[kMaxPSgd];
+  float* params[kMaxPSgd];
+  float* moms[kMaxPSgd];
+};
+
+cudaError_t launch_sgd(const SgdParams& p, uint32_t n_items, bool f16, cudaStream_t stream);
+
 struct StepParams {
   const Xfer* xfers;
   uint32_t* err;

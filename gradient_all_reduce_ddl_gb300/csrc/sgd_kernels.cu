@@ -1,0 +1,245 @@
+// sgd_kernels.cu -- the fused all-reduce followed by the momentum-SGD update.
+//
+// Synchronous data-parallel SGD runs forward, backward, the gradient
+// all-reduce, then the update, every iteration (Baidu write-up, opening
+// paragraph; "索尼发布新的方法...ResNet-50", section "2大方法解决不稳定问题").
+// This pass folds each column of the P gradient buffers in the schedule's
+// order exactly as the fused all-reduce does, rounds the scaled mean to the
+// gradient's storage type, and then -- still in registers -- applies
+//   d = g + wd * p;   v = mu * v + d;   p = p - lr * v
+// to every rank's binary32 parameter and momentum copy, each operation
+// rounded on its own (_rn intrinsics: no fused multiply-add).  The gradient is
+// read once and, if asked, written once; the unfused sequence would read it
+// again for the update.
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+
+namespace ddl {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kV = 2;  // 16-byte gradient columns per thread
+constexpr int kB = 8;  // ranks' loads in flight
+
+__device__ __forceinline__ float round_h(float x) { return __half2float(__float2half_rn(x)); }
+
+template <bool F16>
+__device__ __forceinline__ void unpack(const uint4 r, float* f) {
+  if constexpr (F16) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __half2float(__ushort_as_half((unsigned short)(w[i] & 0xFFFFu)));
+      f[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(w[i] >> 16)));
+    }
+  } else {
+    f[0] = __uint_as_float(r.x);
+    f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z);
+    f[3] = __uint_as_float(r.w);
+  }
+}
+
+template <bool F16>
+__device__ __forceinline__ uint4 pack(const float* f) {
+  if constexpr (F16) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = (uint32_t)__half_as_ushort(__float2half_rn(f[2 * i])) |
+             ((uint32_t)__half_as_ushort(__float2half_rn(f[2 * i + 1])) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+}
+
+// fold one rank's lanes into (in, out): groups of `inner` left-folded, then
+// the group totals; every add rounded to binary16 where a hop carries it,
+// except the last add of the fold
+template <int NL>
+__device__ __forceinline__ void fold_step(float* in, float* out, const float* v, int t, int h, int g, int inner,
+                                          int groups, int P, bool rh) {
+  const bool last = (t == P - 1), gs = (h == 0), ge = (h == inner - 1), fg = (g == 0);
+  const bool rin = rh && !(last && groups == 1), rout = rh && !last;
+#pragma unroll
+  for (int l = 0; l < NL; ++l) {
+    float a = v[l];
+    if (!gs) {
+      a = __fadd_rn(in[l], a);
+      if (rin) a = round_h(a);
+    }
+    in[l] = a;
+    if (ge) {
+      float o = a;
+      if (!fg) {
+        o = __fadd_rn(out[l], a);
+        if (rout) o = round_h(o);
+      }
+      out[l] = o;
+    }
+  }
+}
+
+// the update of one element of one rank; returns the new parameter, writes v
+__device__ __forceinline__ float sgd_one(float g, float pv, float* mv, const SgdParams& p) {
+  const float d = __fadd_rn(g, __fmul_rn(p.wd, pv));
+  const float v = p.has_mom ? __fadd_rn(__fmul_rn(p.mu, *mv), d) : d;
+  *mv = v;
+  return __fsub_rn(pv, __fmul_rn(p.lr, v));
+}
+
+template <bool F16>
+__device__ void sgd_scalar(const SgdParams& p, char* const* gp, float* const* pp, float* const* mp, uint64_t e,
+                           int inner, int groups, bool rh) {
+  float in = 0.f, out = 0.f;
+  int h = 0, g = 0;
+  for (int t = 0; t < p.P; ++t) {
+    const float v = F16 ? __half2float(__ushort_as_half(reinterpret_cast<const unsigned short*>(gp[t])[e]))
+                        : reinterpret_cast<const float*>(gp[t])[e];
+    fold_step<1>(&in, &out, &v, t, h, g, inner, groups, p.P, rh);
+    if (++h == inner) {
+      h = 0;
+      ++g;
+    }
+  }
+  float gm = __fmul_rn(out, p.scale);
+  if (F16) gm = round_h(gm);  // the update reads the gradient as stored
+  for (int t = 0; t < p.P; ++t) {
+    if (p.keep_grads) {
+      if (F16) reinterpret_cast<unsigned short*>(gp[t])[e] = __half_as_ushort(__float2half_rn(gm));
+      else reinterpret_cast<float*>(gp[t])[e] = gm;
+    }
+    float m = p.has_mom ? mp[t][e] : 0.f;
+    pp[t][e] = sgd_one(gm, pp[t][e], &m, p);
+    if (p.has_mom) mp[t][e] = m;
+  }
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_constant__ SgdParams p) {
+  constexpr int L = F16 ? 8 : 4;  // gradient elements per 16-byte column
+  constexpr int Q = L / 4;        // 16-byte binary32 vectors per column of parameters
+  __shared__ char* s_g[kMaxPSgd];
+  __shared__ float* s_p[kMaxPSgd];
+  __shared__ float* s_m[kMaxPSgd];
+  __shared__ Item s_item;
+  __shared__ Segment s_seg;
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
+    const Item it = p.items[p.item0 + blockIdx.x];
+    int ok = it.seg < p.n_segs;
+    Segment sg{0, 1, 1};
+    if (ok) {
+      sg = p.segs[it.seg];
+      ok = (int)sg.inner * (int)sg.groups == p.P && sg.order_off + (uint32_t)p.P <= p.n_orders;
+    }
+    if (!ok) atomicOr(p.err, kErrBadOrder);
+    s_item = it;
+    s_seg = sg;
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  for (int t = threadIdx.x; t < p.P; t += kThreads) {
+    unsigned r = p.orders[s_seg.order_off + t];
+    r = r < (unsigned)p.P ? r : 0;
+    s_g[t] = static_cast<char*>(p.grads[r]);
+    s_p[t] = p.params[r];
+    s_m[t] = p.moms[r];
+  }
+  __syncthreads();
+
+  const int P = p.P, inner = s_seg.inner, groups = s_seg.groups;
+  const bool rh = F16 && p.round_hops;
+  const uint64_t eb = s_item.begin, ee = eb + s_item.len;
+  const uint64_t vb = (eb + L - 1) / L, ve = ee / L;
+  if (!p.vector_ok || vb >= ve) {
+    for (uint64_t e = eb + threadIdx.x; e < ee; e += kThreads) sgd_scalar<F16>(p, s_g, s_p, s_m, e, inner, groups, rh);
+    return;
+  }
+  uint64_t col[kV];
+  bool live[kV];
+#pragma unroll
+  for (int u = 0; u < kV; ++u) {
+    col[u] = vb + threadIdx.x + (uint64_t)u * kThreads;
+    live[u] = col[u] < ve;
+  }
+  float in[kV][L], out[kV][L];
+  int h = 0, g = 0;
+  for (int t0 = 0; t0 < P; t0 += kB) {
+    uint4 raw[kB][kV];
+#pragma unroll
+    for (int j = 0; j < kB; ++j)
+      if (t0 + j < P) {
+#pragma unroll
+        for (int u = 0; u < kV; ++u)
+          raw[j][u] = live[u] ? __ldcs(reinterpret_cast<const uint4*>(s_g[t0 + j]) + col[u]) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+    for (int j = 0; j < kB; ++j)
+      if (t0 + j < P) {
+#pragma unroll
+        for (int u = 0; u < kV; ++u) {
+          float f[L];
+          unpack<F16>(raw[j][u], f);
+          fold_step<L>(in[u], out[u], f, t0 + j, h, g, inner, groups, P, rh);
+        }
+        if (++h == inner) {
+          h = 0;
+          ++g;
+        }
+      }
+  }
+  float gm[kV][L];
+  uint4 res[kV];
+#pragma unroll
+  for (int u = 0; u < kV; ++u) {
+#pragma unroll
+    for (int l = 0; l < L; ++l) gm[u][l] = __fmul_rn(out[u][l], p.scale);
+    res[u] = pack<F16>(gm[u]);
+    if (F16) unpack<F16>(res[u], gm[u]);  // the update reads the gradient as stored
+  }
+#pragma unroll 2
+  for (int t = 0; t < P; ++t) {
+#pragma unroll
+    for (int u = 0; u < kV; ++u) {
+      if (!live[u]) continue;
+      if (p.keep_grads) __stcs(reinterpret_cast<uint4*>(s_g[t]) + col[u], res[u]);
+      float4* pv = reinterpret_cast<float4*>(s_p[t]) + col[u] * Q;
+      float4* mv = p.has_mom ? reinterpret_cast<float4*>(s_m[t]) + col[u] * Q : nullptr;
+      float4 pw[Q], mw[Q];
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        pw[q] = __ldcs(pv + q);
+        mw[q] = p.has_mom ? __ldcs(mv + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        float* pe = reinterpret_cast<float*>(&pw[q]);
+        float* me = reinterpret_cast<float*>(&mw[q]);
+#pragma unroll
+        for (int l = 0; l < 4; ++l) pe[l] = sgd_one(gm[u][q * 4 + l], pe[l], &me[l], p);
+        __stcs(pv + q, pw[q]);
+        if (p.has_mom) __stcs(mv + q, mw[q]);
+      }
+    }
+  }
+  const uint64_t nh = vb * L - eb, nt = ee - ve * L;
+  if (threadIdx.x < nh + nt) {
+    const uint64_t e = threadIdx.x < nh ? eb + threadIdx.x : ve * L + (threadIdx.x - nh);
+    sgd_scalar<F16>(p, s_g, s_p, s_m, e, inner, groups, rh);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_sgd(const SgdParams& p, uint32_t n_items, bool f16, cudaStream_t stream) {
+  if (n_items == 0) return cudaSuccess;
+  if (f16) fold_sgd_kernel<true><<<n_items, kThreads, 0, stream>>>(p);
+  else fold_sgd_kernel<false><<<n_items, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ddl

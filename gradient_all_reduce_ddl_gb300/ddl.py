@@ -38,7 +38,7 @@ EXPORTS = [
     "ddl_allreduce_bucket", "ddl_allreduce_host", "ddl_overlap_begin", "ddl_bucket_ready", "ddl_overlap_end",
     "ddl_plan_num_buckets", "ddl_plan_bucket_range", "ddl_plan_traffic", "ddl_plan_fold_order",
     "ddl_plan_launches", "ddl_plan_check", "ddl_status_string", "ddl_plan_destroy", "ddl_allreduce_noalloc",
-    "ddl_plan_cost", "ddl_plan_set_torus_dims",
+    "ddl_plan_cost", "ddl_plan_set_torus_dims", "ddl_allreduce_sgd",
 ]
 
 
@@ -64,6 +64,7 @@ _sig("ddl_plan_set_torus_dims", _i, _vp, _i, _P(_i))
 _sig("ddl_plan_set_kernel", _i, _vp, _i)
 _sig("ddl_allreduce", _i, _vp, _P(_vp), _f, _vp)
 _sig("ddl_allreduce_bucket", _i, _vp, _i, _P(_vp), _f, _vp)
+_sig("ddl_allreduce_sgd", _i, _vp, _P(_vp), _P(_vp), _P(_vp), _f, _f, _f, _f, _i, _vp)
 _sig("ddl_allreduce_host", _i, _vp, _P(_vp), _P(_vp), _f, _vp)
 _sig("ddl_overlap_begin", _i, _vp, _P(_vp), _f, _vp)
 _sig("ddl_bucket_ready", _i, _vp, _i, _vp)
@@ -146,6 +147,14 @@ def ddl_plan_set_kernel(plan, kernel):
 def ddl_allreduce(plan, rank_bufs, scale, stream=None):
     _ok(_lib.ddl_allreduce(plan, _ptr_array(_dev_ptrs(rank_bufs)), scale, _stream_handle(stream)),
         "ddl_allreduce")
+
+
+def ddl_allreduce_sgd(plan, grad_bufs, param_bufs, mom_bufs, scale, lr, momentum=0.0, weight_decay=0.0,
+                      keep_grads=True, stream=None):
+    moms = None if mom_bufs is None else _ptr_array(_dev_ptrs(mom_bufs))
+    _ok(_lib.ddl_allreduce_sgd(plan, _ptr_array(_dev_ptrs(grad_bufs)), _ptr_array(_dev_ptrs(param_bufs)), moms,
+                               scale, lr, momentum, weight_decay, 1 if keep_grads else 0, _stream_handle(stream)),
+        "ddl_allreduce_sgd")
 
 
 def ddl_allreduce_bucket(plan, bucket, rank_bufs, scale, stream=None):
@@ -269,6 +278,11 @@ class Plan:
 
     def allreduce(self, rank_bufs, scale, stream=None):
         ddl_allreduce(self.handle, rank_bufs, scale, stream)
+
+    def allreduce_sgd(self, grad_bufs, param_bufs, mom_bufs, scale, lr, momentum=0.0, weight_decay=0.0,
+                      keep_grads=True, stream=None):
+        ddl_allreduce_sgd(self.handle, grad_bufs, param_bufs, mom_bufs, scale, lr, momentum, weight_decay,
+                          keep_grads, stream)
 
     def allreduce_bucket(self, bucket, rank_bufs, scale, stream=None):
         ddl_allreduce_bucket(self.handle, bucket, rank_bufs, scale, stream)

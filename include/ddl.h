@@ -152,6 +152,30 @@ ddl_status_t ddl_plan_set_kernel(ddl_plan_t plan, ddl_kernel_t kernel);
  * by the plan) and creates its side stream and events. */
 ddl_status_t ddl_allreduce(ddl_plan_t plan, void* const* rank_bufs, float scale, void* stream);
 
+/* All-reduce followed by the synchronous-SGD update, in the same HBM pass.
+ * Every iteration of synchronous data-parallel SGD runs forward, backward,
+ * the gradient all-reduce and the update (Baidu write-up, opening paragraph);
+ * the pages' own large-batch optimizer (LARS, on the Sony page, "训练设置")
+ * lost its formula, so this is momentum SGD.  After the all-reduce of
+ * grad_bufs (exactly as ddl_allreduce computes it, schedule order, scale),
+ * with g the averaged gradient as stored (binary16 for DDL_FP16), every rank
+ * r updates its own binary32 copies, element by element:
+ *   d = g + weight_decay * p;  v = momentum * v + d;  p = p - lr * v
+ * each product and sum rounded to binary32 on its own (no fused
+ * multiply-add).  This saves the update's second read of the gradient, and
+ * all of the gradient's write-back when keep_grads == 0 (grad_bufs are then
+ * left as they were, not averaged).
+ *  param_bufs: P device arrays of N binary32 parameters, one per rank.
+ *  mom_bufs: P device arrays of N binary32 momenta; NULL only with
+ *    momentum == 0 (then v = d).
+ * All 2P or 3P buffers (with the gradients) must be distinct and
+ * non-overlapping.  Fused and rank-order modes of 1-, 2-level schedules (ring,
+ * multi-ring, 2D torus) with P <= 128; other plans return
+ * DDL_ERR_UNSUPPORTED. */
+ddl_status_t ddl_allreduce_sgd(ddl_plan_t plan, void* const* grad_bufs, float* const* param_bufs,
+                               float* const* mom_bufs, float scale, float lr, float momentum, float weight_decay,
+                               int keep_grads, void* stream);
+
 /* All-reduces bucket b only (0 <= b < ddl_plan_num_buckets). */
 ddl_status_t ddl_allreduce_bucket(ddl_plan_t plan, int bucket, void* const* rank_bufs, float scale,
                                   void* stream);

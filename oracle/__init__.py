@@ -15,6 +15,7 @@ Parity status per function:
   f32_to_f16    pinned (exhaustive against numpy's and the C compiler's binary16)
   ref64         pinned (integer inputs: exact sums)
   cost          pinned (closed forms; the 400 ms language-model example)
+  sgd           pinned (exact dyadic arithmetic; torch.optim.SGD within one rounding)
 
 Buffers are numpy arrays: float32 for fp32, uint16 bit patterns for fp16.
 """
@@ -87,6 +88,9 @@ def _load():
             lib.oracle_ref64.restype = None
             lib.oracle_cost.argtypes = [cfgp, ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
             lib.oracle_cost.restype = ctypes.c_int
+            lib.oracle_sgd.argtypes = [cfgp, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                       ctypes.c_float]
+            lib.oracle_sgd.restype = ctypes.c_int
             lib.oracle_f32_to_f16.argtypes = [P, P, u64]
             lib.oracle_f16_to_f32.argtypes = [P, P, u64]
             lib.oracle_f32_pattern_to_f16.argtypes = [u64, u64, P]
@@ -169,6 +173,17 @@ def cost(cfg: Config, alpha: float, beta: float) -> float:
     t = ctypes.c_double()
     _check(lib.oracle_cost(cfg._ref(), alpha, beta, ctypes.byref(t)))
     return t.value
+
+
+def sgd(cfg: Config, grads, params, moms, scale: float, lr: float, mu: float, wd: float) -> None:
+    """All-reduce ``grads`` (step emulation), then momentum SGD on every
+    rank's fp32 ``params`` and ``moms`` (None when mu == 0), all in place."""
+    lib = _load()
+    for a in list(params) + list(moms or []):
+        assert a.dtype == np.float32 and a.flags.c_contiguous and a.size == cfg.N
+    mp = _ptrs(moms) if moms is not None else None
+    _check(lib.oracle_sgd(cfg._ref(), _ptrs(grads), _ptrs(params), mp, ctypes.c_float(scale),
+                          ctypes.c_float(lr), ctypes.c_float(mu), ctypes.c_float(wd)))
 
 
 def closed_form(cfg: Config, x_rows: np.ndarray, idx: np.ndarray, scale: float) -> np.ndarray:

@@ -652,6 +652,40 @@ int oracle_cost(const oracle_cfg* cfg, double alpha, double beta, double* second
   return 0;
 }
 
+/* The synchronous-SGD update that follows the all-reduce (Baidu write-up,
+ * opening paragraph: each iteration runs forward, backward, the gradient
+ * all-reduce, then the update; the pages' large-batch optimizer is LARS, whose
+ * formula did not survive, so this is plain momentum SGD).  Per rank r and
+ * element i, with g the all-reduced gradient as stored on rank r:
+ *   d = g + wd * p;   v = mu * v + d;   p = p - lr * v
+ * every product and sum rounded to binary32 separately (no fused multiply-add).
+ * The all-reduce runs first, step by step (oracle_emulate); moms may be NULL
+ * when mu == 0 (v is then d). */
+int oracle_sgd(const oracle_cfg* cfg, void* const* grads, float* const* params, float* const* moms, float scale,
+               float lr, float mu, float wd) {
+  Cfg c;
+  const int rc = load_cfg(cfg, c);
+  if (rc) return rc;
+  Bufs b{grads, c.dtype};
+  Emu e(c, &b, scale, -1);
+  e.run();
+  for (int r = 0; r < c.P; ++r) {
+    for (uint64_t i = 0; i < c.N; ++i) {
+      const float g = b.val(r, i);
+      float p = params[r][i];
+      const float d = g + wd * p;
+      float v = d;
+      if (moms) {
+        v = mu * moms[r][i] + d;
+        moms[r][i] = v;
+      }
+      p = p - lr * v;
+      params[r][i] = p;
+    }
+  }
+  return 0;
+}
+
 /* Closed form at sampled elements.  x holds n_idx rows of P values: row s is
  * (rank 0 .. P-1) at element idx[s], in the storage type.  out receives the
  * n_idx results in the storage type. */

@@ -141,6 +141,76 @@ def test_rankorder_within_tolerance(ddl, case, dtype, tol):
         assert np.array_equal(to_numpy_bits(bufs[r]), got0)
 
 
+SGD_CASES = [
+    dict(P=4, N=50_001),
+    dict(P=16, N=70_001, topo="multiring", k=2, bucket_bytes=100_000),
+    dict(P=16, N=99_999, topo="torus", X=4, Y=4),
+    dict(P=32, N=20_000, topo="torus", X=8, Y=4, dtype="f16"),
+    dict(P=8, N=30_011, dtype="f16", bucket_bytes=20_000),
+]
+
+
+@pytest.mark.parametrize("keep", [True, False])
+@pytest.mark.parametrize("mom", [True, False])
+@pytest.mark.parametrize("case", SGD_CASES, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_allreduce_sgd_matches_oracle(ddl, case, mom, keep):
+    w = _w(seed=41, **case)
+    host = _host_inputs(w)
+    rng = np.random.default_rng(7)
+    p0 = rng.standard_normal(w.N).astype(np.float32)
+    v0 = (rng.standard_normal(w.N) * 0.1).astype(np.float32)
+    lr, mu, wd = 0.05, (0.9 if mom else 0.0), 1e-4
+    g_ref = [h.copy() for h in host]
+    p_ref = [p0.copy() for _ in range(w.P)]
+    m_ref = [v0.copy() for _ in range(w.P)] if mom else None
+    oracle.sgd(oracle_cfg(w), g_ref, p_ref, m_ref, w.scale, lr, mu, wd)
+    grads = device_bufs_from_host(host, DEV)
+    params = [torch.from_numpy(p0).to(DEV) for _ in range(w.P)]
+    moms = [torch.from_numpy(v0).to(DEV) for _ in range(w.P)] if mom else None
+    with ddl.Plan.for_workload(w) as plan:
+        plan.allreduce_sgd(grads, params, moms, w.scale, lr, mu, wd, keep_grads=keep)
+        torch.cuda.synchronize()
+        plan.check()
+    for r in range(w.P):
+        assert np.array_equal(params[r].cpu().numpy(), p_ref[r]), ("params", r)
+        if mom:
+            assert np.array_equal(moms[r].cpu().numpy(), m_ref[r]), ("moms", r)
+        assert np.array_equal(to_numpy_bits(grads[r]), g_ref[r] if keep else host[r]), ("grads", r)
+
+
+def test_allreduce_sgd_unaligned_and_errors(ddl):
+    w = _w(P=6, N=12_345, seed=43)
+    host = _host_inputs(w)
+    p0 = np.linspace(-1, 1, w.N, dtype=np.float32)
+    g_ref = [h.copy() for h in host]
+    p_ref = [p0.copy() for _ in range(w.P)]
+    m_ref = [np.zeros(w.N, np.float32) for _ in range(w.P)]
+    oracle.sgd(oracle_cfg(w), g_ref, p_ref, m_ref, w.scale, 0.1, 0.5, 0.01)
+    grads = device_bufs_from_host(host, DEV)
+    big = [torch.zeros(w.N + 1, device=DEV) for _ in range(w.P)]       # parameters 4 bytes off 16-byte alignment
+    params = [b[1:] for b in big]
+    for q in params:
+        q.copy_(torch.from_numpy(p0).to(DEV))
+    moms = [torch.zeros(w.N, device=DEV) for _ in range(w.P)]
+    with ddl.Plan.for_workload(w) as plan:
+        plan.allreduce_sgd(grads, params, moms, w.scale, 0.1, 0.5, 0.01)
+        torch.cuda.synchronize()
+        for r in range(w.P):
+            assert np.array_equal(params[r].cpu().numpy(), p_ref[r])
+            assert np.array_equal(moms[r].cpu().numpy(), m_ref[r])
+        with pytest.raises(ddl.DDLError) as ei:          # momentum without buffers
+            plan.allreduce_sgd(grads, params, None, w.scale, 0.1, 0.5, 0.0)
+        assert ei.value.status == ddl.DDL_ERR_INVALID_ARG
+        with pytest.raises(ddl.DDLError):                # a parameter buffer that is a gradient buffer
+            plan.allreduce_sgd(grads, [grads[0]] + params[1:], moms, w.scale, 0.1, 0.5, 0.0)
+    with ddl.Plan(8, 1000, topo="torus_nd", dims=[2, 2, 2]) as plan:
+        g8 = [torch.zeros(1000, device=DEV) for _ in range(8)]
+        p8 = [torch.zeros(1000, device=DEV) for _ in range(8)]
+        with pytest.raises(ddl.DDLError) as ei:
+            plan.allreduce_sgd(g8, p8, None, 0.125, 0.1)
+        assert ei.value.status == ddl.DDL_ERR_UNSUPPORTED
+
+
 def test_device_generator_matches_host(ddl):
     for dist, dtype, sigma in [("normal", "f32", 1e-3), ("normal", "f16", 1e-2), ("int1000", "f32", 1.0)]:
         w = _w(P=3, N=100_003, dtype=dtype, dist=dist, sigma=sigma, seed=99)

@@ -555,3 +555,62 @@ def test_nd_torus_invalid_dims(oracle_lib):
     for dims in ([3, 3], [0, 8], [2, 2, 2, 1, 1]):
         with pytest.raises(oracle.OracleError):
             oracle.traffic(oracle.Config(P=8, N=10, topo="torus_nd", dims=dims))
+
+
+# --------------------------------------------------------------------------
+# Momentum SGD after the all-reduce
+# --------------------------------------------------------------------------
+
+def test_sgd_exact_dyadic_values(oracle_lib):
+    """Values that are short binary fractions make every product and sum
+    exact, so the result must equal the rational arithmetic exactly:
+    g = mean of the ranks' gradients, d = g + wd p, v = mu v + d, p = p - lr v."""
+    from fractions import Fraction as F
+    P, N = 4, 16
+    rng = np.random.default_rng(9)
+    grads = [(rng.integers(-64, 65, N) / 8).astype(np.float32) for _ in range(P)]
+    p0 = (rng.integers(-32, 33, N) / 4).astype(np.float32)
+    v0 = (rng.integers(-32, 33, N) / 16).astype(np.float32)
+    params = [p0.copy() for _ in range(P)]
+    moms = [v0.copy() for _ in range(P)]
+    lr, mu, wd = 0.125, 0.5, 0.25
+    inputs = [g.copy() for g in grads]
+    oracle.sgd(oracle.Config(P, N), grads, params, moms, 0.25, lr, mu, wd)
+    for i in range(N):
+        g = F(1, 4) * sum(F(float(inputs[r][i])) for r in range(P))   # the mean gradient
+        assert all(F(float(grads[r][i])) == g for r in range(P))       # stored on every rank
+        d = g + F(wd) * F(float(p0[i]))
+        v = F(mu) * F(float(v0[i])) + d
+        p = F(float(p0[i])) - F(lr) * v
+        for r in range(P):
+            assert F(float(moms[r][i])) == v and F(float(params[r][i])) == p
+
+
+def test_sgd_matches_torch_optimizer(oracle_lib):
+    """torch.optim.SGD (momentum, weight decay) on the oracle's all-reduced
+    gradient: an independent implementation; it may fuse a multiply-add, so
+    agreement is to within a couple of binary32 roundings."""
+    torch = pytest.importorskip("torch")
+    P, N = 3, 2000
+    rng = np.random.default_rng(4)
+    grads = [rng.standard_normal(N).astype(np.float32) for _ in range(P)]
+    p0 = rng.standard_normal(N).astype(np.float32)
+    params = [p0.copy() for _ in range(P)]
+    moms = [np.zeros(N, dtype=np.float32) for _ in range(P)]
+    cfg = oracle.Config(P, N, topo="ring")
+    lr, mu, wd = 0.05, 0.9, 1e-4
+    g_ref = [g.copy() for g in grads]
+    oracle.emulate(cfg, g_ref, 1.0 / 3)
+    oracle.sgd(cfg, grads, params, moms, 1.0 / 3, lr, mu, wd)
+    w = torch.nn.Parameter(torch.from_numpy(p0.copy()))
+    opt = torch.optim.SGD([w], lr=lr, momentum=mu, weight_decay=wd)
+    w.grad = torch.from_numpy(g_ref[0].copy())
+    opt.step()
+    got = w.detach().numpy()
+    assert np.allclose(params[0], got, rtol=4e-7, atol=1e-7)
+    assert np.array_equal(grads[0], g_ref[0])
+    # lr = 0 leaves the parameters alone; mu = 0 with no momentum buffer is d
+    params2 = [p0.copy() for _ in range(P)]
+    grads2 = [g.copy() for g in g_ref]
+    oracle.sgd(oracle.Config(P, N), grads2, params2, None, 1.0, 0.0, 0.0, 0.0)
+    assert all(np.array_equal(p, p0) for p in params2)
