@@ -86,10 +86,26 @@ ddl_status_t cuda_status(cudaError_t e) {
   return e == cudaErrorMemoryAllocation ? DDL_ERR_OOM : DDL_ERR_CUDA;
 }
 
-// n-D torus plans fold through the level cascade; others use each
-// segment's (inner, groups).
+// The plan's two-level fold shape: ring, multi-ring and rank order fold one
+// group of P; the torus folds Y groups of X.
+void fold_shape(const Spec& s, int32_t* inner, int32_t* groups) {
+  if (s.mode != ddl::kRankOrder && s.topo == ddl::kTorus) {
+    *inner = s.X;
+    *groups = s.Y;
+  } else if (s.mode != ddl::kRankOrder && s.topo == ddl::kTorusND) {
+    *inner = s.dims[0];
+    *groups = s.P / s.dims[0];
+  } else {
+    *inner = s.P;
+    *groups = 1;
+  }
+}
+
+// n-D torus plans fold through the level cascade (nlev > 0); others use the
+// two-level shape.
 void set_levels(const ddl_plan* p, ddl::FoldParams* fp) {
-  if (p->spec.topo != ddl::kTorusND) return;
+  fold_shape(p->spec, &fp->inner, &fp->groups);
+  if (p->spec.topo != ddl::kTorusND || p->spec.mode == ddl::kRankOrder) return;
   fp->nlev = (int32_t)p->spec.dims.size();
   fp->top = -1;
   for (int l = 0; l < fp->nlev; ++l) {
@@ -444,6 +460,7 @@ ddl_status_t ddl_allreduce_sgd(ddl_plan_t p, void* const* grad_bufs, float* cons
   sp.n_segs = (uint32_t)p->tab.segs.size();
   sp.n_orders = (uint32_t)p->tab.orders.size();
   sp.P = P;
+  fold_shape(p->spec, &sp.inner, &sp.groups);
   sp.scale = scale;
   sp.lr = lr;
   sp.mu = momentum;

@@ -142,30 +142,20 @@ __device__ void fold_scalar(char* const* ptr, uint64_t e, int P, int inner, int 
   for (int t = 0; t < P; ++t) store_elem<F16>(ptr[t], e, r);
 }
 
-// Prologue shared by the fused kernels: fetch the item, check it, and lay out
-// the rank pointers in fold order in shared memory.  Returns false if the
-// item is unusable (the error word is then set).
-__device__ __forceinline__ bool load_item(const FoldParams& p, char** s_ptr, Item* s_item, Segment* s_seg,
-                                          int* s_ok) {
-  if (threadIdx.x == 0) {
-    const Item it = p.items[p.item0 + blockIdx.x];
-    int ok = it.seg < p.n_segs;
-    Segment sg{0, 1, 1};
-    if (ok) {
-      sg = p.segs[it.seg];
-      ok = (int)sg.inner * (int)sg.groups == p.P && sg.order_off + (uint32_t)p.P <= p.n_orders;
-      if (!ok) atomicOr(p.err, kErrBadOrder);
-    } else {
-      atomicOr(p.err, kErrBadItem);
-    }
-    *s_item = it;
-    *s_seg = sg;
-    *s_ok = ok;
+// Prologue shared by the fused kernels: every thread reads the item (one
+// broadcast load), P threads read its rank order and lay the rank pointers out
+// in fold order in shared memory; one barrier.  Returns false (after setting
+// the error word) if the item points outside the tables.
+__device__ __forceinline__ bool load_item(const FoldParams& p, char** s_ptr, Item* item) {
+  *item = p.items[p.item0 + blockIdx.x];
+  const uint64_t off = (uint64_t)item->seg * (uint64_t)p.P;
+  const bool ok = item->seg < p.n_segs && off + (uint64_t)p.P <= p.n_orders;
+  if (!ok) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrBadItem);
+    return false;
   }
-  __syncthreads();
-  if (!*s_ok) return false;
   for (int t = threadIdx.x; t < p.P; t += blockDim.x) {
-    const unsigned r = p.orders[s_seg->order_off + t];
+    const unsigned r = p.orders[off + t];
     s_ptr[t] = static_cast<char*>(p.bufs[r < (unsigned)p.P ? r : 0]);
   }
   __syncthreads();
@@ -191,12 +181,10 @@ __global__ void __launch_bounds__(kThreads, MINB) fold_ldg_kernel(const __grid_c
   static_assert(V * kThreads * 16 >= kTileBytes, "an item must fit one pass of the columns");
   constexpr int L = F16 ? 8 : 4;  // elements per 16-byte column
   __shared__ char* s_ptr[kMaxP];
-  __shared__ Item s_item;
-  __shared__ Segment s_seg;
-  __shared__ int s_ok;
-  if (!load_item(p, s_ptr, &s_item, &s_seg, &s_ok)) return;
+  Item s_item;
+  if (!load_item(p, s_ptr, &s_item)) return;
 
-  const int P = p.P, inner = s_seg.inner, groups = s_seg.groups;
+  const int P = p.P, inner = p.inner, groups = p.groups;
   const bool rh = F16 && p.round_hops;
   const uint64_t eb = s_item.begin, ee = eb + s_item.len;
   const uint64_t vb = (eb + L - 1) / L, ve = ee / L;
@@ -336,10 +324,8 @@ template <bool F16, int B>
 __global__ void __launch_bounds__(kThreads, 2) fold_nd_kernel(const __grid_constant__ FoldParams p) {
   constexpr int L = F16 ? 8 : 4;
   __shared__ char* s_ptr[kMaxP];
-  __shared__ Item s_item;
-  __shared__ Segment s_seg;
-  __shared__ int s_ok;
-  if (!load_item(p, s_ptr, &s_item, &s_seg, &s_ok)) return;
+  Item s_item;
+  if (!load_item(p, s_ptr, &s_item)) return;
   const int P = p.P;
   const bool rh = F16 && p.round_hops;
   const uint64_t eb = s_item.begin, ee = eb + s_item.len;
@@ -567,17 +553,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1) fold_bulk_kernel(const __grid
         m.vb = (m.eb + L - 1) / L;
         m.ve = m.ee / L;
         if (m.ve < m.vb) m.ve = m.vb;
-        m.ok = item.seg < p.n_segs;
-        m.inner = m.groups = 1;
-        m.order_off = 0;
-        if (m.ok) {
-          const Segment sg = p.segs[item.seg];
-          m.ok = (uint32_t)sg.inner * sg.groups == P && sg.order_off + P <= p.n_orders;
-          m.inner = sg.inner;
-          m.groups = sg.groups;
-          m.order_off = sg.order_off;
-        }
-        if (!m.ok) atomicOr(p.err, kErrBadOrder);
+        m.order_off = item.seg * P;
+        m.ok = item.seg < p.n_segs && (uint64_t)item.seg * P + P <= p.n_orders;
+        m.inner = (uint32_t)p.inner;
+        m.groups = (uint32_t)p.groups;
+        if (!m.ok) atomicOr(p.err, kErrBadItem);
         s_meta[k] = m;
       }
       __syncwarp();

@@ -17,9 +17,12 @@ enum : uint32_t {
   kErrBadXfer = 8u       // a message names a rank outside 0..P-1
 };
 
+// Segment s's rank order is orders[s*P .. s*P + P); the fold shape (inner,
+// groups) is the same for every segment of a plan, so kernels read neither
+// the segment records nor more than one table entry before their data.
 struct FoldParams {
   const Item* items;
-  const Segment* segs;
+  const Segment* segs;  // not read by the kernels (kept for the tables' owner)
   const uint8_t* orders;
   uint32_t* err;
   uint32_t item0;      // first item of this launch
@@ -31,9 +34,11 @@ struct FoldParams {
   int32_t vector_ok;   // every rank pointer is 16-byte aligned
   uint32_t n_items;    // items in this launch (persistent kernels)
   uint32_t tile_bytes; // bytes per rank of the largest item
-  int32_t nlev;        // n-D torus: fold levels (0 = use each segment's inner/groups)
+  int32_t nlev;        // n-D torus: fold levels (0 = two-level fold: inner, groups)
   uint16_t lev[kMaxDims];  // level sizes, innermost first (the torus dims)
   int32_t top;         // highest level of size > 1 (its last add is the final one)
+  int32_t inner;       // two-level fold: group length (P for ring / multi-ring, X for the torus)
+  int32_t groups;      // number of groups (1, or Y for the torus)
   int32_t pad2;
   void* bufs[kMaxP];   // rank r's buffer
 };
@@ -42,13 +47,14 @@ struct FoldParams {
 constexpr int kMaxPSgd = 128;
 struct SgdParams {
   const Item* items;
-  const Segment* segs;
+  const Segment* segs;  // not read by the kernel
   const uint8_t* orders;
   uint32_t* err;
   uint32_t item0;
   uint32_t n_segs;
   uint32_t n_orders;
   int32_t P;
+  int32_t inner, groups;  // the plan's two-level fold shape
   float scale, lr, mu, wd;
   int32_t round_hops;
   int32_t vector_ok;   // every buffer 16-byte aligned

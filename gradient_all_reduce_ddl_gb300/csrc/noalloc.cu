@@ -296,6 +296,8 @@ extern "C" ddl_status_t ddl_allreduce_noalloc(int P, size_t N, ddl_dtype_t dtype
   fp.n_segs = (uint32_t)em.n_segs;
   fp.n_orders = (uint32_t)em.n_orders;
   fp.P = P;
+  fp.inner = topo.kind == DDL_TORUS ? topo.X : P;  // the plan's fold shape
+  fp.groups = topo.kind == DDL_TORUS ? topo.Y : 1;
   fp.scale = scale;
   fp.round_hops = pr.esize == 2 ? 1 : 0;
   fp.vector_ok = aligned ? 1 : 0;

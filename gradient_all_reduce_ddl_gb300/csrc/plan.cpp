@@ -408,6 +408,9 @@ bool build_tables(const Spec& s, bool with_steps, Tables* t) {
       bld.step_bucket(b);
       b.step_end = (uint32_t)t->steps.size();
     }
+    // the kernels find segment s's rank order at s * P
+    for (size_t i = 0; i < t->segs.size(); ++i)
+      if (t->segs[i].order_off != (uint64_t)i * (uint64_t)s.P) return false;
     return true;
   } catch (const std::bad_alloc&) {
     *t = Tables();

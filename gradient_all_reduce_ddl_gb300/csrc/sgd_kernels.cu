@@ -124,26 +124,14 @@ __global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_cons
   __shared__ char* s_g[kMaxPSgd];
   __shared__ float* s_p[kMaxPSgd];
   __shared__ float* s_m[kMaxPSgd];
-  __shared__ Item s_item;
-  __shared__ Segment s_seg;
-  __shared__ int s_ok;
-  if (threadIdx.x == 0) {
-    const Item it = p.items[p.item0 + blockIdx.x];
-    int ok = it.seg < p.n_segs;
-    Segment sg{0, 1, 1};
-    if (ok) {
-      sg = p.segs[it.seg];
-      ok = (int)sg.inner * (int)sg.groups == p.P && sg.order_off + (uint32_t)p.P <= p.n_orders;
-    }
-    if (!ok) atomicOr(p.err, kErrBadOrder);
-    s_item = it;
-    s_seg = sg;
-    s_ok = ok;
+  const Item s_item = p.items[p.item0 + blockIdx.x];  // one broadcast load
+  const uint64_t off = (uint64_t)s_item.seg * (uint64_t)p.P;
+  if (!(s_item.seg < p.n_segs && off + (uint64_t)p.P <= p.n_orders)) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrBadItem);
+    return;
   }
-  __syncthreads();
-  if (!s_ok) return;
   for (int t = threadIdx.x; t < p.P; t += kThreads) {
-    unsigned r = p.orders[s_seg.order_off + t];
+    unsigned r = p.orders[off + t];
     r = r < (unsigned)p.P ? r : 0;
     s_g[t] = static_cast<char*>(p.grads[r]);
     s_p[t] = p.params[r];
@@ -151,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_cons
   }
   __syncthreads();
 
-  const int P = p.P, inner = s_seg.inner, groups = s_seg.groups;
+  const int P = p.P, inner = p.inner, groups = p.groups;
   const bool rh = F16 && p.round_hops;
   const uint64_t eb = s_item.begin, ee = eb + s_item.len;
   const uint64_t vb = (eb + L - 1) / L, ve = ee / L;

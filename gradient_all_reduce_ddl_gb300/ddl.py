@@ -255,6 +255,7 @@ class Plan:
     def __init__(self, P, N, dtype="f32", topo="ring", k=1, X=0, Y=0, bucket_bytes=0, layers=None,
                  mode="fused", kernel="auto", dims=None):
         self.P, self.N, self.dtype = int(P), int(N), dtype
+        self._last_ptrs, self._last_arr = None, None
         topo_t = ddl_topology_t(TOPOLOGIES[topo], int(k), int(X), int(Y))
         self.handle = ddl_plan_create(self.P, self.N, DTYPES[dtype], topo_t, int(bucket_bytes))
         try:
@@ -277,7 +278,11 @@ class Plan:
                    layers=w.layers, dims=getattr(w, "dims", None), **kw)
 
     def allreduce(self, rank_bufs, scale, stream=None):
-        ddl_allreduce(self.handle, rank_bufs, scale, stream)
+        # the ctypes pointer array is rebuilt only when the buffers change
+        ptrs = tuple(_dev_ptrs(rank_bufs))
+        if ptrs != self._last_ptrs:
+            self._last_ptrs, self._last_arr = ptrs, _ptr_array(ptrs)
+        _ok(_lib.ddl_allreduce(self.handle, self._last_arr, scale, _stream_handle(stream)), "ddl_allreduce")
 
     def allreduce_sgd(self, grad_bufs, param_bufs, mom_bufs, scale, lr, momentum=0.0, weight_decay=0.0,
                       keep_grads=True, stream=None):
