@@ -347,6 +347,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--elems", type=int, default=0,
+                    help="run the workload with this many elements per rank (no layer list): small cases "
+                         "for profiling")
     ap.add_argument("--overlap", action="store_true",
                     help="also time a synthetic backward overlapped with the bucketed all-reduce")
     ap.add_argument("--sgd", action="store_true",
@@ -358,6 +361,8 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = synth.WORKLOADS[args.workload]
+    if args.elems:
+        w = w.with_(N=args.elems, layers=None, name=f"{w.name}@{args.elems}")
     if args.impl == "reference":
         return run_reference(args, w)
 

@@ -189,30 +189,41 @@ __global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_cons
     res[u] = pack<F16>(gm[u]);
     if (F16) unpack<F16>(res[u], gm[u]);  // the update reads the gradient as stored
   }
-#pragma unroll 2
-  for (int t = 0; t < P; ++t) {
+  // the update: parameter and momentum loads of kUB ranks in flight at once
+  constexpr int kUB = F16 ? 1 : 4;  // fp16 columns carry twice the parameters
+  for (int t0 = 0; t0 < P; t0 += kUB) {
+    float4 pw[kUB][kV][Q], mw[kUB][kV][Q];
 #pragma unroll
-    for (int u = 0; u < kV; ++u) {
-      if (!live[u]) continue;
-      if (p.keep_grads) __stcs(reinterpret_cast<uint4*>(s_g[t]) + col[u], res[u]);
-      float4* pv = reinterpret_cast<float4*>(s_p[t]) + col[u] * Q;
-      float4* mv = p.has_mom ? reinterpret_cast<float4*>(s_m[t]) + col[u] * Q : nullptr;
-      float4 pw[Q], mw[Q];
+    for (int j = 0; j < kUB; ++j)
 #pragma unroll
-      for (int q = 0; q < Q; ++q) {
-        pw[q] = __ldcs(pv + q);
-        mw[q] = p.has_mom ? __ldcs(mv + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      for (int u = 0; u < kV; ++u)
+        if (t0 + j < P && live[u]) {
+          const float4* pv = reinterpret_cast<const float4*>(s_p[t0 + j]) + col[u] * Q;
+          const float4* mv = reinterpret_cast<const float4*>(s_m[t0 + j]) + col[u] * Q;
 #pragma unroll
-      for (int q = 0; q < Q; ++q) {
-        float* pe = reinterpret_cast<float*>(&pw[q]);
-        float* me = reinterpret_cast<float*>(&mw[q]);
+          for (int q = 0; q < Q; ++q) {
+            pw[j][u][q] = __ldcs(pv + q);
+            mw[j][u][q] = p.has_mom ? __ldcs(mv + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
 #pragma unroll
-        for (int l = 0; l < 4; ++l) pe[l] = sgd_one(gm[u][q * 4 + l], pe[l], &me[l], p);
-        __stcs(pv + q, pw[q]);
-        if (p.has_mom) __stcs(mv + q, mw[q]);
-      }
-    }
+    for (int j = 0; j < kUB; ++j)
+#pragma unroll
+      for (int u = 0; u < kV; ++u)
+        if (t0 + j < P && live[u]) {
+          if (p.keep_grads) __stcs(reinterpret_cast<uint4*>(s_g[t0 + j]) + col[u], res[u]);
+          float4* pv = reinterpret_cast<float4*>(s_p[t0 + j]) + col[u] * Q;
+          float4* mv = reinterpret_cast<float4*>(s_m[t0 + j]) + col[u] * Q;
+#pragma unroll
+          for (int q = 0; q < Q; ++q) {
+            float* pe = reinterpret_cast<float*>(&pw[j][u][q]);
+            float* me = reinterpret_cast<float*>(&mw[j][u][q]);
+#pragma unroll
+            for (int l = 0; l < 4; ++l) pe[l] = sgd_one(gm[u][q * 4 + l], pe[l], &me[l], p);
+            __stcs(pv + q, pw[j][u][q]);
+            if (p.has_mom) __stcs(mv + q, mw[j][u][q]);
+          }
+        }
   }
   const uint64_t nh = vb * L - eb, nt = ee - ve * L;
   if (threadIdx.x < nh + nt) {
