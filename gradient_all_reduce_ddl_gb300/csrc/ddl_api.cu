@@ -5,8 +5,10 @@
 // arguments before queueing anything, maps CUDA failures to DDL_ERR_CUDA, and
 // never throws across the ABI.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstring>
 #include <new>
 #include <string>
@@ -192,8 +194,21 @@ ddl_status_t check_bufs(ddl_plan* p, void* const* bufs, bool device_check, bool*
   return DDL_OK;
 }
 
+// An NVTX range per bucket, so a timeline shows which bucket each launch
+// reduced (costs nothing measurable without a tool attached).
+struct BucketRange {
+  BucketRange(int b, const ddl::Bucket& bk) {
+    char name[96];
+    std::snprintf(name, sizeof(name), "ddl bucket %d [%llu, %llu)", b, (unsigned long long)bk.lo,
+                  (unsigned long long)bk.hi);
+    nvtxRangePushA(name);
+  }
+  ~BucketRange() { nvtxRangePop(); }
+};
+
 ddl_status_t run_bucket(ddl_plan* p, int b, void* const* bufs, bool aligned, float scale, cudaStream_t s) {
   const ddl::Bucket& bk = p->tab.buckets[b];
+  const BucketRange range(b, bk);
   const bool f16 = p->spec.esize == 2;
   if (p->spec.mode == ddl::kStepwise) {
     ddl::StepParams sp;
