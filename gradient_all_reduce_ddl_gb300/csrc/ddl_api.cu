@@ -116,11 +116,14 @@ void set_levels(const ddl_plan* p, ddl::FoldParams* fp) {
   }
 }
 
-// Work-item size for the plan's kernel: the n-D pass takes one column per
-// thread (<= 4 KB per rank); the staged passes fill ~64 KB per stage.
+// Work-item size for the plan's kernel: the n-D pass covers 8 KB (fp32) or
+// 4 KB (fp16) per rank per CTA; the staged passes fill ~64 KB per stage.
 uint32_t choose_tile(const Spec& s, int kernel) {
   const uint32_t ldg = ddl::ldg_tile_bytes(s.N * (uint64_t)s.esize);
-  if (s.topo == ddl::kTorusND) return ldg < 4096u ? ldg : 4096u;
+  if (s.topo == ddl::kTorusND) {
+    const uint32_t cap = s.esize == 2 ? 4096u : 8192u;  // the n-D pass's columns per thread
+    return ldg < cap ? ldg : cap;
+  }
   if (kernel == DDL_KERNEL_BULK || kernel == DDL_KERNEL_BULK_LOAD) return ddl::bulk_tile_bytes(s.P);
   return ldg;
 }

@@ -259,8 +259,8 @@ __global__ void __launch_bounds__(kThreads, MINB) fold_ldg_kernel(const __grid_c
 // level follows the ranks in fold order: a finished group of level l is added
 // into level l+1.  Every add is rounded to binary16 where a hop would carry
 // it, except the final add (the last one at the highest level of size > 1).
-// One column per thread (fp16 keeps 4 levels x 8 lanes of accumulators), so
-// the plan's items are at most 4 KB per rank.
+// fp32 takes two columns per thread (items up to 8 KB per rank); fp16, whose
+// 4 levels x 8 lanes of accumulators fill the registers, takes one (4 KB).
 // ---------------------------------------------------------------------------
 // One accumulator per level (levels written out, so every index is a
 // compile-time constant and the accumulators live in registers); NL lanes.
@@ -320,7 +320,7 @@ __device__ __forceinline__ void fold_nd_scalar(const FoldParams& p, char* const*
   for (int t = 0; t < p.P; ++t) store_elem<F16>(ptr[t], e, r);
 }
 
-template <bool F16, int B>
+template <bool F16, int V, int B>
 __global__ void __launch_bounds__(kThreads, 2) fold_nd_kernel(const __grid_constant__ FoldParams p) {
   constexpr int L = F16 ? 8 : 4;
   __shared__ char* s_ptr[kMaxP];
@@ -335,33 +335,52 @@ __global__ void __launch_bounds__(kThreads, 2) fold_nd_kernel(const __grid_const
     for (uint64_t e = eb + threadIdx.x; e < ee; e += kThreads) fold_nd_scalar<F16>(p, s_ptr, e, rh);
     return;
   }
-  if (ve - vb > (uint64_t)kThreads) {  // one column per thread: items must be <= 4 KB per rank
+  if (ve - vb > (uint64_t)V * kThreads) {  // V columns per thread cover the largest item
     if (threadIdx.x == 0) atomicOr(p.err, kErrBadItem);
     return;
   }
-  const uint64_t col = vb + threadIdx.x;
-  if (col < ve) {
-    Cascade<L> cs;
-    for (int t0 = 0; t0 < P; t0 += B) {
-      uint4 raw[B];
+  uint64_t col[V];
+  bool live[V];
 #pragma unroll
-      for (int j = 0; j < B; ++j)
-        if (t0 + j < P) raw[j] = __ldcs(reinterpret_cast<const uint4*>(s_ptr[t0 + j]) + col);
+  for (int u = 0; u < V; ++u) {
+    col[u] = vb + threadIdx.x + (uint64_t)u * kThreads;
+    live[u] = col[u] < ve;
+  }
+  Cascade<L> cs[V];
+  for (int t0 = 0; t0 < P; t0 += B) {
+    uint4 raw[B][V];
 #pragma unroll
-      for (int j = 0; j < B; ++j) {
-        if (t0 + j < P) {
+    for (int j = 0; j < B; ++j)
+      if (t0 + j < P) {
+#pragma unroll
+        for (int u = 0; u < V; ++u)
+          raw[j][u] = live[u] ? __ldcs(reinterpret_cast<const uint4*>(s_ptr[t0 + j]) + col[u]) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+    for (int j = 0; j < B; ++j) {
+      if (t0 + j < P) {
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
           float f[L];
-          unpack<F16>(raw[j], f);
-          cs.push(f, t0 + j == P - 1, p, rh);
+          unpack<F16>(raw[j][u], f);
+          cs[u].push(f, t0 + j == P - 1, p, rh);
         }
       }
     }
+  }
+  uint4 res[V];
+#pragma unroll
+  for (int u = 0; u < V; ++u) {
     float r[L];
-    cs.result(r, p.nlev);
+    cs[u].result(r, p.nlev);
 #pragma unroll
     for (int l = 0; l < L; ++l) r[l] = __fmul_rn(r[l], p.scale);
-    const uint4 res = pack<F16>(r);
-    for (int t = 0; t < P; ++t) __stcs(reinterpret_cast<uint4*>(s_ptr[t]) + col, res);
+    res[u] = pack<F16>(r);
+  }
+  for (int t = 0; t < P; ++t) {
+#pragma unroll
+    for (int u = 0; u < V; ++u)
+      if (live[u]) __stcs(reinterpret_cast<uint4*>(s_ptr[t]) + col[u], res[u]);
   }
   const uint64_t nh = vb * L - eb, nt = ee - ve * L;
   if (threadIdx.x < nh + nt) {
@@ -699,8 +718,9 @@ cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t strea
 cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream) {
   if (n_items == 0) return cudaSuccess;
   if (p.nlev > 0) {  // n-D torus: the level-cascade register pass
-    if (f16) fold_nd_kernel<true, 8><<<n_items, kThreads, 0, stream>>>(p);
-    else fold_nd_kernel<false, 8><<<n_items, kThreads, 0, stream>>>(p);
+    // fp32: two columns per thread (items up to 8 KB); fp16: one (up to 4 KB)
+    if (f16) fold_nd_kernel<true, 1, 8><<<n_items, kThreads, 0, stream>>>(p);
+    else fold_nd_kernel<false, 2, 8><<<n_items, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
   }
   if (variant == kVarBulk)
