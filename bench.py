@@ -128,7 +128,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside)}
 
 
-def cpu_baseline(w, target_s: float = 6.0, max_elems: int = 2_000_000):
+def cpu_baseline(w, target_s: float = 10.0, max_elems: int = 2_000_000):
     """The oracle as it stands (single thread) on a bounded sample of the
     workload: same P, schedule, dtype and value distribution, the first
     `max_elems` elements per rank as one bucket; repeated until `target_s`."""

@@ -390,6 +390,32 @@ def test_allreduce_host_zero_copy(ddl, dtype):
             assert e.status == ddl.DDL_ERR_INVALID_ARG
 
 
+def test_allreduce_captured_in_cuda_graph(ddl):
+    """After a first (uploading) call, ddl_allreduce can be captured in a CUDA
+    graph; each replay reduces whatever the buffers hold at that time."""
+    w = _w(P=16, N=77_777, topo="torus", X=4, Y=4, bucket_bytes=100_000, seed=51)
+    host = _host_inputs(w)
+    ref = [h.copy() for h in host]
+    oracle.emulate(oracle_cfg(w), ref, w.scale)
+    bufs = device_bufs_from_host(host, DEV)
+    src = [b.clone() for b in bufs]
+    with ddl.Plan.for_workload(w) as plan:
+        plan.allreduce(bufs, w.scale)          # uploads the tables, outside the capture
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            plan.allreduce(bufs, w.scale, s)
+        for _ in range(2):                     # replay twice on fresh inputs
+            for b, x in zip(bufs, src):
+                b.copy_(x)
+            g.replay()
+            torch.cuda.synchronize()
+            for r in range(w.P):
+                assert np.array_equal(to_numpy_bits(bufs[r]), ref[r]), r
+
+
 def test_launch_counts_and_checks(ddl):
     w = _w(P=16, N=100_000, topo="torus", X=4, Y=4, bucket_bytes=100_000)
     bufs = device_bufs_generated(w, DEV)
