@@ -9,7 +9,10 @@
 namespace ddl {
 
 constexpr int kMaxP = 256;          // rank orders are stored as bytes
-constexpr int kTileBytes = 8192;    // bytes per rank in one fused work item
+#ifndef DDL_TILE_BYTES
+#define DDL_TILE_BYTES 8192
+#endif
+constexpr int kTileBytes = DDL_TILE_BYTES;  // bytes per rank in one fused work item (<= 8192)
 
 // One contiguous run of elements whose fold order is the same.  The ranks are
 // added in the order orders[order_off .. order_off+P), as `groups` groups of
