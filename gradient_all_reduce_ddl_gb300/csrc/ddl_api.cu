@@ -713,6 +713,15 @@ ddl_status_t ddl_plan_check(ddl_plan_t p) {
   return DDL_ERR_DEVICE_CHECK;
 }
 
+ddl_status_t ddl_selftest_wait_timeout(ddl_plan_t p, uint32_t limit_us, void* stream) {
+  if (!p || limit_us == 0 || limit_us > 1000000) return DDL_ERR_INVALID_ARG;
+  const ddl_status_t st = ensure_device(p);
+  if (st != DDL_OK) return st;
+  const cudaError_t e =
+      ddl::launch_wait_timeout_selftest(p->d_err, (uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream));
+  return cuda_status(e);
+}
+
 const char* ddl_status_string(ddl_status_t s) {
   switch (s) {
     case DDL_OK: return "DDL_OK";

@@ -456,15 +456,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait for the phase with the given parity to complete: gives up
+// after limit_ns of wall time (or 2^28 polls) and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < (1u << 28); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 63u && global_ns() - t0 > kWaitNs) break;
+    if ((i & 63u) == 63u && global_ns() - t0 > limit_ns) break;
   }
   return false;
+}
+
+// Exercises the bounded wait's give-up path: one CTA waits on an mbarrier
+// that nothing arrives at, with a short limit, and records the timeout in
+// the error word exactly as the staged kernels do.
+__global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, limit_ns)) atomicOr(err, kErrWaitTimeout);
 }
 
 __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -714,6 +728,11 @@ cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t strea
 }
 
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream) {
   if (n_items == 0) return cudaSuccess;

@@ -81,6 +81,7 @@ struct StepParams {
 enum FoldVariant : int { kVarLdg = 1, kVarBulk = 2, kVarBulkLoad = 3 };
 
 cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream);
+cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, uint32_t n_xfers, uint64_t max_len, bool f16, cudaStream_t stream);
 
 }  // namespace ddl

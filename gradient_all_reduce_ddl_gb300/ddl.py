@@ -38,7 +38,7 @@ EXPORTS = [
     "ddl_allreduce_bucket", "ddl_allreduce_host", "ddl_overlap_begin", "ddl_bucket_ready", "ddl_overlap_end",
     "ddl_plan_num_buckets", "ddl_plan_bucket_range", "ddl_plan_traffic", "ddl_plan_fold_order",
     "ddl_plan_launches", "ddl_plan_check", "ddl_status_string", "ddl_plan_destroy", "ddl_allreduce_noalloc",
-    "ddl_plan_cost", "ddl_plan_set_torus_dims", "ddl_allreduce_sgd",
+    "ddl_plan_cost", "ddl_plan_set_torus_dims", "ddl_allreduce_sgd", "ddl_selftest_wait_timeout",
 ]
 
 
@@ -76,6 +76,7 @@ _sig("ddl_plan_cost", _i, _vp, ctypes.c_double, ctypes.c_double, _P(ctypes.c_dou
 _sig("ddl_plan_fold_order", _i, _vp, _sz, _P(ctypes.c_int32), _P(ctypes.c_int32), _P(ctypes.c_int32))
 _sig("ddl_plan_launches", _i, _vp, _P(_u64))
 _sig("ddl_plan_check", _i, _vp)
+_sig("ddl_selftest_wait_timeout", _i, _vp, ctypes.c_uint32, _vp)
 _sig("ddl_status_string", ctypes.c_char_p, _i)
 _sig("ddl_plan_destroy", _i, _vp)
 _sig("ddl_allreduce_noalloc", _i, _i, _sz, _i, ddl_topology_t, _sz, _i, _P(_sz), _P(_vp), _f, _vp)
@@ -221,6 +222,10 @@ def ddl_plan_launches(plan):
 
 def ddl_plan_check(plan):
     return _lib.ddl_plan_check(plan)
+
+
+def ddl_selftest_wait_timeout(plan, limit_us, stream=None):
+    _ok(_lib.ddl_selftest_wait_timeout(plan, limit_us, _stream_handle(stream)), "ddl_selftest_wait_timeout")
 
 
 def ddl_plan_destroy(plan):

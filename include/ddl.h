@@ -270,6 +270,15 @@ ddl_status_t ddl_plan_launches(ddl_plan_t plan, uint64_t* n);
  * ran out (the word is then cleared), DDL_OK otherwise. */
 ddl_status_t ddl_plan_check(ddl_plan_t plan);
 
+/* Self-test of the bounded waits in the staged kernels: queues one CTA that
+ * waits on an mbarrier nothing arrives at, gives up after limit_us
+ * microseconds (1..1,000,000) and records the timeout in the plan's error
+ * word, as a staged pass whose copies never completed would.  The next
+ * ddl_plan_check then returns DDL_ERR_DEVICE_CHECK and clears the word; the
+ * CUDA context stays usable.  The pages have no counterpart: this checks the
+ * library's own failure path without faulting or hanging the GPU. */
+ddl_status_t ddl_selftest_wait_timeout(ddl_plan_t plan, uint32_t limit_us, void* stream);
+
 /* A static string for a status code. */
 const char* ddl_status_string(ddl_status_t status);
 

@@ -416,6 +416,29 @@ def test_allreduce_captured_in_cuda_graph(ddl):
                 assert np.array_equal(to_numpy_bits(bufs[r]), ref[r]), r
 
 
+def test_bounded_wait_timeout_is_reported_and_context_survives(ddl):
+    """A wait that runs out (an mbarrier nothing arrives at, 50 ms limit)
+    sets the error word; ddl_plan_check reports DDL_ERR_DEVICE_CHECK once,
+    and the next all-reduce on the same context is still bit-exact."""
+    w = _w(P=4, N=20_001, seed=61)
+    host = _host_inputs(w)
+    ref = [h.copy() for h in host]
+    oracle.emulate(oracle_cfg(w), ref, w.scale)
+    with ddl.Plan.for_workload(w, kernel="bulk") as plan:
+        assert ddl.ddl_plan_check(plan.handle) == ddl.DDL_OK
+        ddl.ddl_selftest_wait_timeout(plan.handle, 50_000)
+        assert ddl.ddl_plan_check(plan.handle) == ddl.DDL_ERR_DEVICE_CHECK
+        assert ddl.ddl_plan_check(plan.handle) == ddl.DDL_OK        # the word was cleared
+        bufs = device_bufs_from_host(host, DEV)
+        plan.allreduce(bufs, w.scale)
+        torch.cuda.synchronize()
+        assert ddl.ddl_plan_check(plan.handle) == ddl.DDL_OK
+        for r in range(w.P):
+            assert np.array_equal(to_numpy_bits(bufs[r]), ref[r])
+        with pytest.raises(ddl.DDLError):
+            ddl.ddl_selftest_wait_timeout(plan.handle, 0)
+
+
 def test_launch_counts_and_checks(ddl):
     w = _w(P=16, N=100_000, topo="torus", X=4, Y=4, bucket_bytes=100_000)
     bufs = device_bufs_generated(w, DEV)
