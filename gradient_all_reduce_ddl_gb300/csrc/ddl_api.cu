@@ -197,6 +197,39 @@ ddl_status_t check_bufs(ddl_plan* p, void* const* bufs, bool device_check, bool*
   return DDL_OK;
 }
 
+// Fused pass over items [ia, ib): a whole bucket, or a tile-aligned element range of one.
+ddl_status_t run_items(ddl_plan* p, uint32_t ia, uint32_t ib, void* const* bufs, bool aligned, float scale,
+                       cudaStream_t s) {
+  if (ib <= ia) return DDL_OK;
+  const bool f16 = p->spec.esize == 2;
+  ddl::FoldParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.items = p->d_items;
+  fp.segs = p->d_segs;
+  fp.orders = p->d_orders;
+  fp.err = p->d_err;
+  fp.item0 = ia;
+  fp.n_segs = (uint32_t)p->tab.segs.size();
+  fp.n_orders = (uint32_t)p->tab.orders.size();
+  fp.P = p->spec.P;
+  fp.scale = scale;
+  fp.round_hops = (f16 && p->spec.mode == ddl::kFused) ? 1 : 0;
+  fp.vector_ok = aligned ? 1 : 0;
+  for (int r = 0; r < p->spec.P; ++r) fp.bufs[r] = bufs[r];
+  // the staged passes need 16-byte aligned buffers; otherwise the register
+  // pass runs (its element-wise path), with the same results
+  int variant = ddl::kVarLdg;
+  if (aligned && p->kernel == DDL_KERNEL_BULK) variant = ddl::kVarBulk;
+  if (aligned && p->kernel == DDL_KERNEL_BULK_LOAD) variant = ddl::kVarBulkLoad;
+  fp.n_items = ib - ia;
+  fp.tile_bytes = p->spec.tile_bytes;
+  set_levels(p, &fp);
+  const cudaError_t e = ddl::launch_fold(fp, ib - ia, f16, variant, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  ++p->launches;
+  return DDL_OK;
+}
+
 // An NVTX range per bucket, so a timeline shows which bucket each launch
 // reduced (costs nothing measurable without a tool attached).
 struct BucketRange {
@@ -231,65 +264,7 @@ ddl_status_t run_bucket(ddl_plan* p, int b, void* const* bufs, bool aligned, flo
     }
     return DDL_OK;
   }
-  ddl::FoldParams fp;
-  std::memset(&fp, 0, sizeof(fp));
-  fp.items = p->d_items;
-  fp.segs = p->d_segs;
-  fp.orders = p->d_orders;
-  fp.err = p->d_err;
-  fp.item0 = bk.item_begin;
-  fp.n_segs = (uint32_t)p->tab.segs.size();
-  fp.n_orders = (uint32_t)p->tab.orders.size();
-  fp.P = p->spec.P;
-  fp.scale = scale;
-  fp.round_hops = (f16 && p->spec.mode == ddl::kFused) ? 1 : 0;
-  fp.vector_ok = aligned ? 1 : 0;
-  for (int r = 0; r < p->spec.P; ++r) fp.bufs[r] = bufs[r];
-  // the staged pass needs 16-byte aligned buffers; otherwise the register
-  // pass runs (its element-wise path), with the same results
-  int variant = ddl::kVarLdg;
-  if (aligned && p->kernel == DDL_KERNEL_BULK) variant = ddl::kVarBulk;
-  if (aligned && p->kernel == DDL_KERNEL_BULK_LOAD) variant = ddl::kVarBulkLoad;
-  const uint32_t n = bk.item_end - bk.item_begin;
-  if (n == 0) return DDL_OK;
-  fp.n_items = n;
-  fp.tile_bytes = p->spec.tile_bytes;
-  set_levels(p, &fp);
-  const cudaError_t e = ddl::launch_fold(fp, n, f16, variant, s);
-  if (e != cudaSuccess) return cuda_status(e);
-  ++p->launches;
-  return DDL_OK;
-}
-
-// Fused pass over items [ia, ib) of bucket b only (an element range of it).
-ddl_status_t run_items(ddl_plan* p, uint32_t ia, uint32_t ib, void* const* bufs, bool aligned, float scale,
-                       cudaStream_t s) {
-  if (ib <= ia) return DDL_OK;
-  const bool f16 = p->spec.esize == 2;
-  ddl::FoldParams fp;
-  std::memset(&fp, 0, sizeof(fp));
-  fp.items = p->d_items;
-  fp.segs = p->d_segs;
-  fp.orders = p->d_orders;
-  fp.err = p->d_err;
-  fp.item0 = ia;
-  fp.n_segs = (uint32_t)p->tab.segs.size();
-  fp.n_orders = (uint32_t)p->tab.orders.size();
-  fp.P = p->spec.P;
-  fp.scale = scale;
-  fp.round_hops = (f16 && p->spec.mode == ddl::kFused) ? 1 : 0;
-  fp.vector_ok = aligned ? 1 : 0;
-  for (int r = 0; r < p->spec.P; ++r) fp.bufs[r] = bufs[r];
-  int variant = ddl::kVarLdg;
-  if (aligned && p->kernel == DDL_KERNEL_BULK) variant = ddl::kVarBulk;
-  if (aligned && p->kernel == DDL_KERNEL_BULK_LOAD) variant = ddl::kVarBulkLoad;
-  fp.n_items = ib - ia;
-  fp.tile_bytes = p->spec.tile_bytes;
-  set_levels(p, &fp);
-  const cudaError_t e = ddl::launch_fold(fp, ib - ia, f16, variant, s);
-  if (e != cudaSuccess) return cuda_status(e);
-  ++p->launches;
-  return DDL_OK;
+  return run_items(p, bk.item_begin, bk.item_end, bufs, aligned, scale, s);
 }
 
 // First item of bucket b that starts at or after element x.
@@ -408,16 +383,18 @@ ddl_status_t ddl_plan_set_torus_dims(ddl_plan_t p, int ndims, const int* dims) {
 ddl_status_t ddl_plan_set_kernel(ddl_plan_t p, ddl_kernel_t k) {
   if (!p || p->ov_active || k < DDL_KERNEL_AUTO || k > DDL_KERNEL_BULK_LOAD) return DDL_ERR_INVALID_ARG;
   const uint32_t tile = choose_tile(p->spec, (int)k);
-  p->kernel = (int)k;
-  if (tile == p->spec.tile_bytes) return DDL_OK;
-  const Spec old = p->spec;
-  p->spec.tile_bytes = tile;
-  const ddl_status_t st = rebuild(p);
-  if (st != DDL_OK) {
-    p->spec = old;
-    rebuild(p);
+  if (tile != p->spec.tile_bytes) {
+    const Spec old = p->spec;
+    p->spec.tile_bytes = tile;
+    const ddl_status_t st = rebuild(p);
+    if (st != DDL_OK) {
+      p->spec = old;
+      rebuild(p);
+      return st;
+    }
   }
-  return st;
+  p->kernel = (int)k;
+  return DDL_OK;
 }
 
 ddl_status_t ddl_allreduce(ddl_plan_t p, void* const* bufs, float scale, void* stream) {
@@ -444,15 +421,18 @@ ddl_status_t ddl_allreduce_sgd(ddl_plan_t p, void* const* grad_bufs, float* cons
   bool aligned = false;
   ddl_status_t st = prepare(p, grad_bufs, &aligned);
   if (st != DDL_OK) return st;
-  // parameters and momenta: distinct, non-overlapping binary32 device arrays
-  std::vector<void*> cur(param_bufs, param_bufs + P);
+  // parameters and momenta: distinct binary32 device arrays that overlap
+  // neither each other nor the gradients (the check is cached per full set)
+  std::vector<void*> cur(grad_bufs, grad_bufs + P);
+  cur.insert(cur.end(), param_bufs, param_bufs + P);
   if (mom_bufs) cur.insert(cur.end(), mom_bufs, mom_bufs + P);
   if (p->checked_sgd != cur) {
     const uint64_t gbytes = p->spec.N * (uint64_t)p->spec.esize, fbytes = p->spec.N * 4ull;
     std::vector<std::pair<uintptr_t, uint64_t>> all;
     for (int r = 0; r < P; ++r) all.push_back({reinterpret_cast<uintptr_t>(grad_bufs[r]), gbytes});
     bool al = true;
-    for (void* q : cur) {
+    for (size_t i = (size_t)P; i < cur.size(); ++i) {
+      void* q = cur[i];
       if (!q) return DDL_ERR_INVALID_ARG;
       all.push_back({reinterpret_cast<uintptr_t>(q), fbytes});
       al = al && (reinterpret_cast<uintptr_t>(q) % 16 == 0);
@@ -549,7 +529,6 @@ ddl_status_t ddl_allreduce_host(ddl_plan_t p, void* const* host_bufs, void* cons
   bool aligned = false;
   ddl_status_t st = prepare(p, dev_bufs, &aligned);
   if (st != DDL_OK) return st;
-  if (p->ov_active) return DDL_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t es = (size_t)p->spec.esize;
   const int P = p->spec.P;

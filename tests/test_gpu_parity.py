@@ -203,6 +203,8 @@ def test_allreduce_sgd_unaligned_and_errors(ddl):
         assert ei.value.status == ddl.DDL_ERR_INVALID_ARG
         with pytest.raises(ddl.DDLError):                # a parameter buffer that is a gradient buffer
             plan.allreduce_sgd(grads, [grads[0]] + params[1:], moms, w.scale, 0.1, 0.5, 0.0)
+        with pytest.raises(ddl.DDLError):                # new gradients that overlap the cached parameters
+            plan.allreduce_sgd([params[0]] + grads[1:], params, moms, w.scale, 0.1, 0.5, 0.0)
     with ddl.Plan(8, 1000, topo="torus_nd", dims=[2, 2, 2]) as plan:
         g8 = [torch.zeros(1000, device=DEV) for _ in range(8)]
         p8 = [torch.zeros(1000, device=DEV) for _ in range(8)]
