@@ -459,7 +459,8 @@ def main():
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": None if achieved is None else round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": None if achieved is None else round(achieved / peak, 4),
                 "peak_kind": f"hbm_gbs of {peak_kind}", "traffic": traffic,
-                "algorithmic_bytes_per_launch": nbytes // max(1, nb), "launches_per_step": launches_per_call,
+                "algorithmic_bytes_per_launch": nbytes // max(1, launches_per_call),
+                "launches_per_step": launches_per_call,
                 "avg_call_ms": round(avg_call_ms, 4)}
 
     # end to end through the C ABI with page-locked host buffers

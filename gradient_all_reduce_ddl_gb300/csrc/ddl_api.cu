@@ -402,8 +402,17 @@ ddl_status_t ddl_allreduce(ddl_plan_t p, void* const* bufs, float scale, void* s
   ddl_status_t st = prepare(p, bufs, &aligned);
   if (st != DDL_OK) return st;
   if (p->ov_active) return DDL_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p->spec.mode != ddl::kStepwise && p->tab.buckets.size() > 1) {
+    // every bucket back to back: one launch over all work items (stored
+    // bucket by bucket, so bucket 0's CTAs still start first)
+    nvtxRangePushA("ddl all buckets");
+    st = run_items(p, 0, (uint32_t)p->tab.items.size(), bufs, aligned, scale, s);
+    nvtxRangePop();
+    return st;
+  }
   for (int b = 0; b < (int)p->tab.buckets.size(); ++b) {
-    st = run_bucket(p, b, bufs, aligned, scale, static_cast<cudaStream_t>(stream));
+    st = run_bucket(p, b, bufs, aligned, scale, s);
     if (st != DDL_OK) return st;
   }
   return DDL_OK;
@@ -472,13 +481,12 @@ ddl_status_t ddl_allreduce_sgd(ddl_plan_t p, void* const* grad_bufs, float* cons
     sp.params[r] = param_bufs[r];
     sp.moms[r] = mom_bufs ? mom_bufs[r] : nullptr;
   }
-  for (const ddl::Bucket& bk : p->tab.buckets) {
-    sp.item0 = bk.item_begin;
-    const cudaError_t e =
-        ddl::launch_sgd(sp, bk.item_end - bk.item_begin, p->spec.esize == 2, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_status(e);
-    ++p->launches;
-  }
+  // every bucket in one launch (items are stored bucket by bucket)
+  sp.item0 = 0;
+  const cudaError_t e =
+      ddl::launch_sgd(sp, (uint32_t)p->tab.items.size(), p->spec.esize == 2, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status(e);
+  ++p->launches;
   return DDL_OK;
 }
 

@@ -141,7 +141,8 @@ ddl_status_t ddl_plan_set_mode(ddl_plan_t plan, ddl_mode_t mode);
  * identical for every variant.  Host-only. */
 ddl_status_t ddl_plan_set_kernel(ddl_plan_t plan, ddl_kernel_t kernel);
 
-/* All-reduces every bucket, in place, in issue order.
+/* All-reduces every bucket, in place, in issue order (fused and rank-order
+ * modes: one launch covering every bucket's work, bucket 0's first).
  *  rank_bufs: host array of P device pointers, rank r's N elements (binary32,
  *    or binary16 for DDL_FP16).  The buffers must be distinct and must not
  *    overlap; the caller owns them and keeps them valid until the queued work

@@ -446,11 +446,15 @@ def test_launch_counts_and_checks(ddl):
     bufs = device_bufs_generated(w, DEV)
     with ddl.Plan.for_workload(w) as plan:
         nb = plan.num_buckets
+        assert nb > 1
         plan.allreduce(bufs, w.scale)
-        assert plan.launches == nb
+        assert plan.launches == 1                      # every bucket in one fused launch
+        for b in range(nb):
+            plan.allreduce_bucket(b, bufs, w.scale)
+        assert plan.launches == 1 + nb
         plan.set_mode("stepwise")
         plan.allreduce(bufs, w.scale)
-        assert plan.launches == nb + nb * (2 * 3 + 2 * 3)
+        assert plan.launches == 1 + nb + nb * (2 * 3 + 2 * 3)
         torch.cuda.synchronize()
         plan.check()
         # a host pointer is not device memory: refused before any launch
