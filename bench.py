@@ -343,7 +343,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--mode", default="fused", choices=["fused", "stepwise", "rankorder"])
-    ap.add_argument("--kernel", default="auto", choices=["auto", "ldg", "bulk", "bulkload"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "ldg", "bulk", "bulkload", "tma"])
+    ap.add_argument("--slab", action="store_true",
+                    help="rank buffers in one slab (ddl_allreduce_slab); needed by --kernel tma")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -382,11 +384,20 @@ def main():
 
     tdt = torch.float16 if w.dtype == "f16" else torch.float32
     bufs = []
+    slab = None
+    stride_elems = (w.N + 63) // 64 * 64  # 256-byte aligned rank rows in the slab
+    if args.slab:
+        slab = torch.empty(w.P * stride_elems, dtype=tdt, device=dev)
     for r in range(w.P):
-        t = torch.empty(w.N, dtype=tdt, device=dev)
+        t = slab[r * stride_elems: r * stride_elems + w.N] if slab is not None else \
+            torch.empty(w.N, dtype=tdt, device=dev)
         synth.fill_device(t.data_ptr(), w.N, w.seed, r, w.dist, w.sigma, w.dtype, stream=stream.cuda_stream)
         bufs.append(t)
     plan = ddl.Plan.for_workload(w, mode=args.mode, kernel=args.kernel)
+    if slab is not None:
+        slab_stride = stride_elems * w.esize
+        plan.allreduce = (lambda b, sc, st=None, _p=plan:
+                          _p.allreduce_slab(slab, slab_stride, sc, st))
     nbytes = w.min_bytes
 
     def barrier():
@@ -449,7 +460,9 @@ def main():
     # the call's average device time is this replica's timed region / steps
     avg_call_ms = local_ms / args.steps
     peak, peak_kind = measured_peak()
-    kernel_name = {"fused": "fold_bulk_kernel" if args.kernel in ("bulk", "bulkload") else "fold_ldg_kernel",
+    kernel_name = {"fused": {"bulk": "fold_bulk_kernel", "bulkload": "fold_bulk_kernel",
+                             "tma": "fold_tma_kernel" if args.slab else "fold_ldg_kernel"}.get(args.kernel,
+                                                                                            "fold_ldg_kernel"),
                    "rankorder": "fold_ldg_kernel (rank order)", "stepwise": "step_kernel"}[args.mode]
     if args.mode == "stepwise":
         achieved = None
@@ -528,6 +541,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
                 "config": {"workload": w.name, "P": w.P, "N": w.N, "schedule": schedule_name(w), "mode": args.mode,
                            "kernel": args.kernel, "buckets": nb, "bytes_per_step": nbytes,
+                           "layout": "one slab (ddl_allreduce_slab)" if args.slab else "P separate buffers",
                            "launch": (f"CUDA graph replay, {per_graph} all-reduces per graph" if args.graph
                                       else "ddl_allreduce call per step"),
                            "elems_per_s": round(elems, 1), "frac_of_hbm": round(gbs / ws / peak, 4),

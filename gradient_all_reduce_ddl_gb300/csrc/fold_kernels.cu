@@ -700,6 +700,178 @@ __global__ void __launch_bounds__(kBulkThreads, 1) fold_bulk_kernel(const __grid
   }
 }
 
+// ---------------------------------------------------------------------------
+// Variant 4: staged through shared memory by 2D tensor-map copies.  When the
+// P rank buffers are equally spaced (one slab, rank r at base + r * stride), a
+// tensor map of [P rows x N elements] lets one cp.async.bulk.tensor.2d fetch
+// a box of every rank's next `box_elems` elements at once: P times fewer copy
+// requests than one 1D bulk copy per rank.  Otherwise as variant 3: one
+// producer warp, 8 consumer warps, a 3-stage mbarrier ring, bounded waits,
+// results stored from registers.  Box x coordinates are multiples of 16 bytes
+// (item columns start 16-byte aligned); boxes running past the tensor's end
+// read zeros, and bytes beyond the item are loaded but never used.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tensor_load_2d(void* dst_smem, const CUtensorMap* map, int32_t x, int32_t y,
+                                               uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_addr(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(kBulkThreads, 1)
+    fold_tma_kernel(const __grid_constant__ FoldParams p, const __grid_constant__ CUtensorMap tmap) {
+  constexpr int L = F16 ? 8 : 4;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const uint32_t P = (uint32_t)p.P, T = p.tile_bytes;
+  const uint32_t BW = p.box_elems * (F16 ? 2u : 4u);  // bytes of one rank's row in a box
+  unsigned char* stage = smem;
+  uint8_t* s_order = stage + (uint32_t)kStages * P * T + 2u * T;
+  BulkMeta* s_meta = reinterpret_cast<BulkMeta*>(s_order + kStages * kMaxP);
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_meta + kStages);
+  uint64_t* empty = full + kStages;
+
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
+  const uint32_t my_n = p.n_items > blockIdx.x ? (p.n_items - 1u - blockIdx.x) / gridDim.x + 1u : 0u;
+  const bool rh = F16 && p.round_hops;
+
+  if (tid == 0) {
+    for (int k = 0; k < kStages; ++k) {
+      mbar_init(&full[k], 1);
+      mbar_init(&empty[k], kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+  }
+  __syncthreads();
+
+  uint32_t issued = 0, consumed = 0;
+  bool timed_out = false;
+
+  if (warp == kConsumerWarps) {
+    for (uint32_t s = 0; s < my_n; ++s) {
+      const uint32_t k = s % kStages;
+      if (s >= (uint32_t)kStages && !mbar_wait(&empty[k], ((s / kStages) - 1u) & 1u)) {
+        timed_out = true;
+        break;
+      }
+      if (lane == 0) {
+        const Item item = p.items[p.item0 + blockIdx.x + s * gridDim.x];
+        BulkMeta m;
+        m.eb = item.begin;
+        m.ee = item.begin + item.len;
+        m.vb = (m.eb + L - 1) / L;
+        m.ve = m.ee / L;
+        if (m.ve < m.vb) m.ve = m.vb;
+        m.order_off = item.seg * P;
+        m.ok = item.seg < p.n_segs && (uint64_t)item.seg * P + P <= p.n_orders && (m.ve - m.vb) * 16u <= T;
+        m.inner = (uint32_t)p.inner;
+        m.groups = (uint32_t)p.groups;
+        if (!m.ok) atomicOr(p.err, kErrBadItem);
+        s_meta[k] = m;
+      }
+      __syncwarp();
+      const BulkMeta m = s_meta[k];
+      if (m.ok)
+        for (uint32_t t = lane; t < P; t += 32) {
+          const uint32_t r = p.orders[m.order_off + t];
+          s_order[k * kMaxP + t] = (uint8_t)(r < P ? r : 0);
+        }
+      const uint32_t bytes = m.ok ? (uint32_t)(m.ve - m.vb) * 16u : 0u;
+      const uint32_t nbox = (bytes + BW - 1) / BW;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&full[k], nbox * P * BW);  // release: meta and order published
+      __syncwarp();
+      for (uint32_t j = lane; j < nbox; j += 32)
+        tensor_load_2d(stage + (size_t)k * P * T + (size_t)j * P * BW, &tmap,
+                       (int32_t)(m.vb * L + (uint64_t)j * p.box_elems), 0, &full[k]);
+      issued = s + 1;
+    }
+    if (timed_out && lane == 0) atomicOr(p.err, kErrWaitTimeout);
+  } else {
+    for (uint32_t s = 0; s < my_n; ++s) {
+      const uint32_t k = s % kStages;
+      if (!mbar_wait(&full[k], (s / kStages) & 1u)) {
+        timed_out = true;
+        break;
+      }
+      const BulkMeta m = s_meta[k];
+      const uint8_t* ord = s_order + k * kMaxP;
+      const uint32_t ncols = (uint32_t)(m.ve - m.vb);
+      if (m.ok) {
+        const unsigned char* st = stage + (size_t)k * P * T;
+        for (uint32_t c = tid; c < ncols; c += kConsumers) {
+          const uint32_t o = c * 16u, box = o / BW, within = o % BW;
+          const unsigned char* col = st + (size_t)box * P * BW + within;
+          float in[L], out[L];
+          int h = 0, g = 0;
+          for (uint32_t t0 = 0; t0 < P; t0 += 8) {
+            uint4 raw[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (t0 + q < P) raw[q] = *reinterpret_cast<const uint4*>(col + (size_t)ord[t0 + q] * BW);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (t0 + q < P) {
+                float f[L];
+                unpack<F16>(raw[q], f);
+                const Ctl ctl = ctl_at((int)(t0 + q), h, g, (int)m.inner, (int)m.groups, (int)P, rh);
+                fold_lanes<L>(in, out, f, ctl);
+                if (++h == (int)m.inner) {
+                  h = 0;
+                  ++g;
+                }
+              }
+            }
+          }
+          float r[L];
+#pragma unroll
+          for (int l = 0; l < L; ++l) r[l] = __fmul_rn(out[l], p.scale);
+          const uint4 res = pack<F16>(r);
+          for (uint32_t t = 0; t < P; ++t) __stcs(reinterpret_cast<uint4*>(p.bufs[t]) + m.vb + c, res);
+        }
+        const uint64_t nh = (m.ve > m.vb) ? m.vb * L - m.eb : m.ee - m.eb;
+        const uint64_t nt = (m.ve > m.vb) ? m.ee - m.ve * L : 0;
+        if (tid < nh + nt) {
+          const uint64_t e = tid < nh ? m.eb + tid : m.ve * L + (tid - nh);
+          fold_scalar_ordered<F16>(p, ord, e, (int)m.inner, (int)m.groups, rh);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[k]);
+      consumed = s + 1;
+    }
+    if (timed_out && lane == 0) atomicOr(p.err, kErrWaitTimeout);
+  }
+  __shared__ uint32_t s_issued, s_consumed;
+  if (warp == kConsumerWarps && lane == 0) s_issued = issued;
+  if (tid == 0) s_consumed = consumed;
+  __syncthreads();
+  if (tid == 0)
+    for (uint32_t q = s_consumed; q < s_issued; ++q) mbar_wait(&full[q % kStages], (q / kStages) & 1u);
+}
+
+template <bool F16>
+cudaError_t launch_tma(const FoldParams& p, const CUtensorMap& tmap, uint32_t n_items, cudaStream_t stream) {
+  const uint32_t smem = bulk_smem_bytes((uint32_t)p.P, p.tile_bytes);
+  int dev = 0, sms = 0, max_smem = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  const uint32_t es = F16 ? 2u : 4u;
+  if (smem > (uint32_t)max_smem || p.box_elems == 0 || p.box_elems > 256 || (p.box_elems * es) % 16 != 0 ||
+      p.tile_bytes % (p.box_elems * es) != 0)
+    return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(fold_tma_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const uint32_t grid = n_items < (uint32_t)sms ? n_items : (uint32_t)sms;
+  fold_tma_kernel<F16><<<grid, kBulkThreads, smem, stream>>>(p, tmap);
+  return cudaGetLastError();
+}
+
 template <bool F16, bool kBulkStore>
 cudaError_t launch_bulk(const FoldParams& p, uint32_t n_items, cudaStream_t stream) {
   const uint32_t smem = bulk_smem_bytes((uint32_t)p.P, p.tile_bytes);
@@ -728,6 +900,12 @@ cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t strea
 }
 
 }  // namespace
+
+cudaError_t launch_fold_tma(const FoldParams& p, const CUtensorMap& tmap, uint32_t n_items, bool f16,
+                            cudaStream_t stream) {
+  if (n_items == 0) return cudaSuccess;
+  return f16 ? launch_tma<true>(p, tmap, n_items, stream) : launch_tma<false>(p, tmap, n_items, stream);
+}
 
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream) {
   wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(err, limit_ns);

@@ -1,6 +1,7 @@
 // kernels.h -- launch records of the all-reduce kernels (internal).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (a type only; the encoder is fetched at run time)
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -39,7 +40,7 @@ struct FoldParams {
   int32_t top;         // highest level of size > 1 (its last add is the final one)
   int32_t inner;       // two-level fold: group length (P for ring / multi-ring, X for the torus)
   int32_t groups;      // number of groups (1, or Y for the torus)
-  int32_t pad2;
+  uint32_t box_elems;  // tensor-map pass: box width in elements (box height = P)
   void* bufs[kMaxP];   // rank r's buffer
 };
 
@@ -79,6 +80,11 @@ struct StepParams {
 
 // Variants of the fused pass.
 enum FoldVariant : int { kVarLdg = 1, kVarBulk = 2, kVarBulkLoad = 3 };
+
+// The staged pass whose loads are 2D tensor-map copies of [P ranks x box]
+// from equally spaced rank buffers (ddl_allreduce_slab).
+cudaError_t launch_fold_tma(const FoldParams& p, const CUtensorMap& tmap, uint32_t n_items, bool f16,
+                            cudaStream_t stream);
 
 cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);

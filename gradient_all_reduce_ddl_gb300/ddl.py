@@ -31,7 +31,7 @@ DDL_RING, DDL_MULTIRING, DDL_TORUS = 0, 1, 2
 # ddl_mode_t
 DDL_MODE_FUSED, DDL_MODE_STEPWISE, DDL_MODE_RANKORDER = 0, 1, 2
 # ddl_kernel_t
-DDL_KERNEL_AUTO, DDL_KERNEL_LDG, DDL_KERNEL_BULK, DDL_KERNEL_BULK_LOAD = 0, 1, 2, 3
+DDL_KERNEL_AUTO, DDL_KERNEL_LDG, DDL_KERNEL_BULK, DDL_KERNEL_BULK_LOAD, DDL_KERNEL_TMA = 0, 1, 2, 3, 4
 
 EXPORTS = [
     "ddl_plan_create", "ddl_plan_set_layers", "ddl_plan_set_mode", "ddl_plan_set_kernel", "ddl_allreduce",
@@ -39,6 +39,7 @@ EXPORTS = [
     "ddl_plan_num_buckets", "ddl_plan_bucket_range", "ddl_plan_traffic", "ddl_plan_fold_order",
     "ddl_plan_launches", "ddl_plan_check", "ddl_status_string", "ddl_plan_destroy", "ddl_allreduce_noalloc",
     "ddl_plan_cost", "ddl_plan_set_torus_dims", "ddl_allreduce_sgd", "ddl_selftest_wait_timeout",
+    "ddl_allreduce_slab",
 ]
 
 
@@ -64,6 +65,7 @@ _sig("ddl_plan_set_torus_dims", _i, _vp, _i, _P(_i))
 _sig("ddl_plan_set_kernel", _i, _vp, _i)
 _sig("ddl_allreduce", _i, _vp, _P(_vp), _f, _vp)
 _sig("ddl_allreduce_bucket", _i, _vp, _i, _P(_vp), _f, _vp)
+_sig("ddl_allreduce_slab", _i, _vp, _vp, _sz, _f, _vp)
 _sig("ddl_allreduce_sgd", _i, _vp, _P(_vp), _P(_vp), _P(_vp), _f, _f, _f, _f, _i, _vp)
 _sig("ddl_allreduce_host", _i, _vp, _P(_vp), _P(_vp), _f, _vp)
 _sig("ddl_overlap_begin", _i, _vp, _P(_vp), _f, _vp)
@@ -156,6 +158,12 @@ def ddl_allreduce_sgd(plan, grad_bufs, param_bufs, mom_bufs, scale, lr, momentum
     _ok(_lib.ddl_allreduce_sgd(plan, _ptr_array(_dev_ptrs(grad_bufs)), _ptr_array(_dev_ptrs(param_bufs)), moms,
                                scale, lr, momentum, weight_decay, 1 if keep_grads else 0, _stream_handle(stream)),
         "ddl_allreduce_sgd")
+
+
+def ddl_allreduce_slab(plan, base, rank_stride_bytes, scale, stream=None):
+    """base: device pointer (or tensor) of the slab; rank r at base + r * stride."""
+    ptr = base.data_ptr() if hasattr(base, "data_ptr") else int(base)
+    _ok(_lib.ddl_allreduce_slab(plan, ptr, rank_stride_bytes, scale, _stream_handle(stream)), "ddl_allreduce_slab")
 
 
 def ddl_allreduce_bucket(plan, bucket, rank_bufs, scale, stream=None):
@@ -251,7 +259,8 @@ def ddl_allreduce_noalloc(P, N, dtype, topology, bucket_bytes, layers, rank_bufs
 TOPOLOGIES = {"ring": DDL_RING, "multiring": DDL_MULTIRING, "torus": DDL_TORUS, "torus_nd": DDL_RING}
 DTYPES = {"f32": DDL_FP32, "f16": DDL_FP16}
 MODES = {"fused": DDL_MODE_FUSED, "stepwise": DDL_MODE_STEPWISE, "rankorder": DDL_MODE_RANKORDER}
-KERNELS = {"auto": DDL_KERNEL_AUTO, "ldg": DDL_KERNEL_LDG, "bulk": DDL_KERNEL_BULK, "bulkload": DDL_KERNEL_BULK_LOAD}
+KERNELS = {"auto": DDL_KERNEL_AUTO, "ldg": DDL_KERNEL_LDG, "bulk": DDL_KERNEL_BULK, "bulkload": DDL_KERNEL_BULK_LOAD,
+           "tma": DDL_KERNEL_TMA}
 
 
 class Plan:
@@ -293,6 +302,9 @@ class Plan:
                       keep_grads=True, stream=None):
         ddl_allreduce_sgd(self.handle, grad_bufs, param_bufs, mom_bufs, scale, lr, momentum, weight_decay,
                           keep_grads, stream)
+
+    def allreduce_slab(self, base, rank_stride_bytes, scale, stream=None):
+        ddl_allreduce_slab(self.handle, base, rank_stride_bytes, scale, stream)
 
     def allreduce_bucket(self, bucket, rank_bufs, scale, stream=None):
         ddl_allreduce_bucket(self.handle, bucket, rank_bufs, scale, stream)

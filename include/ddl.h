@@ -92,7 +92,10 @@ typedef enum {
   DDL_KERNEL_LDG = 1,   /* fused pass with 16-byte register loads and stores */
   DDL_KERNEL_BULK = 2,  /* fused pass staged through shared memory by bulk async copies,
                            loads and stores */
-  DDL_KERNEL_BULK_LOAD = 3  /* bulk async loads into shared memory, stores from registers */
+  DDL_KERNEL_BULK_LOAD = 3, /* bulk async loads into shared memory, stores from registers */
+  DDL_KERNEL_TMA = 4        /* ddl_allreduce_slab only: 2D tensor-map loads of every rank's
+                               next tile in one copy, stores from registers (elsewhere and
+                               when the slab does not qualify: the register pass) */
 } ddl_kernel_t;
 
 typedef struct ddl_plan* ddl_plan_t;
@@ -176,6 +179,18 @@ ddl_status_t ddl_allreduce(ddl_plan_t plan, void* const* rank_bufs, float scale,
 ddl_status_t ddl_allreduce_sgd(ddl_plan_t plan, void* const* grad_bufs, float* const* param_bufs,
                                float* const* mom_bufs, float scale, float lr, float momentum, float weight_decay,
                                int keep_grads, void* stream);
+
+/* ddl_allreduce for rank buffers laid out in one slab: rank r's N elements
+ * start at base + r * rank_stride_bytes (rank_stride_bytes >= N * element
+ * size; the slab is caller-owned device memory).  Results equal
+ * ddl_allreduce's on the same buffers.  With DDL_KERNEL_TMA, a 2D tensor map
+ * over the slab (P rows, stride rank_stride_bytes) lets one
+ * cp.async.bulk.tensor copy bring a tile of every rank into shared memory.
+ * That path needs a 16-byte aligned base and stride, N < 2^31, a fused or
+ * rank-order plan of a ring, multi-ring or 2D torus, and P <= 256; otherwise
+ * the call runs the register pass.  The tensor map is encoded on the first
+ * call for a given slab and kept by the plan. */
+ddl_status_t ddl_allreduce_slab(ddl_plan_t plan, void* base, size_t rank_stride_bytes, float scale, void* stream);
 
 /* All-reduces bucket b only (0 <= b < ddl_plan_num_buckets). */
 ddl_status_t ddl_allreduce_bucket(ddl_plan_t plan, int bucket, void* const* rank_bufs, float scale,

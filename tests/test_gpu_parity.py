@@ -244,6 +244,46 @@ def test_oracle_binary16_rounding_equals_device_conversion():
         _check_narrow(prefix | np.uint32(low))
 
 
+SLAB_CASES = [
+    dict(P=4, N=50_003),
+    dict(P=16, N=99_999, topo="torus", X=4, Y=4),
+    dict(P=32, N=33_333, topo="torus", X=8, Y=4, dtype="f16"),
+    dict(P=64, N=20_011, topo="multiring", k=4, bucket_bytes=30_000),
+    dict(P=128, N=5_003),
+    dict(P=12, N=40_000, topo="torus", X=3, Y=4, bucket_bytes=50_000, dtype="f16"),
+    dict(P=8, N=30_001, topo="torus_nd", dims=[2, 2, 2]),
+]
+
+
+@pytest.mark.parametrize("kernel", ["tma", "ldg", "bulkload"])
+@pytest.mark.parametrize("case", SLAB_CASES, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_slab_matches_oracle(ddl, case, kernel):
+    """Rank buffers in one slab (rank r at base + r * stride): the 2D
+    tensor-map pass and the other kernels give the oracle's bits."""
+    w = _w(seed=71, **case)
+    host = _host_inputs(w)
+    ref = [h.copy() for h in host]
+    oracle.emulate(oracle_cfg(w), ref, w.scale)
+    es = w.esize
+    for pad in (0, 24):                           # pad 24 B: stride not a multiple of 16 -> register pass
+        stride = (w.N * es + 255) // 256 * 256 + pad
+        slab = torch.zeros(stride * w.P // 2 + 16, dtype=torch.int16, device=DEV)
+        base = slab.data_ptr()
+        bufs = []
+        for r in range(w.P):
+            t = slab.view(torch.uint8)[r * stride: r * stride + w.N * es].view(torch_dtype(w.dtype))
+            t.copy_(device_bufs_from_host([host[r]], DEV)[0])
+            bufs.append(t)
+        with ddl.Plan.for_workload(w, kernel=kernel) as plan:
+            plan.allreduce_slab(base, stride, w.scale)
+            torch.cuda.synchronize()
+            plan.check()
+            for r in range(w.P):
+                assert np.array_equal(to_numpy_bits(bufs[r]), ref[r]), (pad, r)
+            with pytest.raises(ddl.DDLError):     # ranks would overlap
+                plan.allreduce_slab(base, w.N * es - 16, w.scale)
+
+
 def test_device_generator_matches_host(ddl):
     for dist, dtype, sigma in [("normal", "f32", 1e-3), ("normal", "f16", 1e-2), ("int1000", "f32", 1.0)]:
         w = _w(P=3, N=100_003, dtype=dtype, dist=dist, sigma=sigma, seed=99)
