@@ -105,6 +105,40 @@ __device__ __forceinline__ void fold_lanes(float* in, float* out, const float* v
   }
 }
 
+// Packed binary16 hop adds.  For binary16 a and b, fl16(fl32(a + b)) equals
+// the correctly rounded fl16(a + b): binary32 carries 24 >= 2*11 + 2
+// significand bits, the bound under which double rounding of a sum is
+// innocuous (S. A. Figueroa, "When is double rounding innocuous?", SIGNUM
+// Newsletter 30(3), 1995), and every binary16 sum is inside binary32's
+// exponent range.  So a hop add whose result is rounded to binary16 is one
+// add.rn.f16x2 per two lanes, bit for bit the same as widen + add + round.
+__device__ __forceinline__ uint32_t hadd2_rn(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// One fold position that is not the last (every add rounded to binary16), on
+// a 16-byte column of binary16 pairs.
+__device__ __forceinline__ void fold_h2(uint32_t* in, uint32_t* out, const uint4 v, const Ctl& c) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t a = w[i];
+    if (!c.group_start) a = hadd2_rn(in[i], a);
+    in[i] = a;
+    if (c.group_end) out[i] = c.first_group ? a : hadd2_rn(out[i], a);
+  }
+}
+
+__device__ __forceinline__ void widen_h2(const uint32_t* h, float* f) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __half2float(__ushort_as_half((unsigned short)(h[i] & 0xFFFFu)));
+    f[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(h[i] >> 16)));
+  }
+}
+
 template <bool F16>
 __device__ __forceinline__ float load_elem(const char* base, uint64_t e) {
   if constexpr (F16) {
@@ -176,8 +210,11 @@ __device__ __forceinline__ bool load_item(const FoldParams& p, char** s_ptr, Ite
 #define DDL_LDG_MINB 2
 #endif
 
-template <bool F16, int V, int B, int MINB>
+// H2: binary16 with rounded hops; every position but the last folds packed
+// pairs (fold_h2), the last one widens and takes its final add in binary32.
+template <bool F16, bool H2, int V, int B, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB) fold_ldg_kernel(const __grid_constant__ FoldParams p) {
+  static_assert(F16 || !H2, "packed hops are binary16 only");
   static_assert(V * kThreads * 16 >= kTileBytes, "an item must fit one pass of the columns");
   constexpr int L = F16 ? 8 : 4;  // elements per 16-byte column
   __shared__ char* s_ptr[kMaxP];
@@ -203,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, MINB) fold_ldg_kernel(const __grid_c
     live[u] = col[u] < ve;
   }
   float in[V][L], out[V][L];
+  uint32_t hin[V][4] = {}, hout[V][4] = {};  // packed accumulators (H2)
   int h = 0, g = 0;
   for (int t0 = 0; t0 < P; t0 += B) {
     uint4 raw[B][V];
@@ -220,6 +258,14 @@ __global__ void __launch_bounds__(kThreads, MINB) fold_ldg_kernel(const __grid_c
         const Ctl c = ctl_at(t0 + j, h, g, inner, groups, P, rh);
 #pragma unroll
         for (int u = 0; u < V; ++u) {
+          if constexpr (H2) {
+            if (t0 + j < P - 1) {
+              fold_h2(hin[u], hout[u], raw[j][u], c);
+              continue;
+            }
+            widen_h2(hin[u], in[u]);  // the last position: its final add stays binary32
+            widen_h2(hout[u], out[u]);
+          }
           float f[L];
           unpack<F16>(raw[j][u], f);
           fold_lanes<L>(in[u], out[u], f, c);
@@ -892,9 +938,12 @@ cudaError_t launch_bulk(const FoldParams& p, uint32_t n_items, cudaStream_t stre
 template <bool F16>
 cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t stream) {
   if constexpr (F16) {
-    fold_ldg_kernel<true, 2, DDL_LDG_F16_B, DDL_LDG_MINB><<<n_items, kThreads, 0, stream>>>(p);
+    if (p.round_hops)
+      fold_ldg_kernel<true, true, 2, DDL_LDG_F16_B, DDL_LDG_MINB><<<n_items, kThreads, 0, stream>>>(p);
+    else
+      fold_ldg_kernel<true, false, 2, DDL_LDG_F16_B, DDL_LDG_MINB><<<n_items, kThreads, 0, stream>>>(p);
   } else {
-    fold_ldg_kernel<false, 2, DDL_LDG_F32_B, DDL_LDG_MINB><<<n_items, kThreads, 0, stream>>>(p);
+    fold_ldg_kernel<false, false, 2, DDL_LDG_F32_B, DDL_LDG_MINB><<<n_items, kThreads, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }

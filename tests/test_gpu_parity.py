@@ -244,6 +244,43 @@ def test_oracle_binary16_rounding_equals_device_conversion():
         _check_narrow(prefix | np.uint32(low))
 
 
+def test_packed_hop_add_over_every_binary16_pair(ddl):
+    """Every binary16 pair (a, b) through one hop add of the fused pass.
+
+    A 3-rank fp16 ring whose rank 2 holds -0 everywhere, scale 1: chunk 0
+    folds (a + b, rounded to binary16 for the next hop) + (-0), and that last
+    add and the scale leave the hop value as it is.  So chunk 0 must equal
+    fl16(fl32(a) + fl32(b)), computed here by torch on the device (widen, add
+    in binary32, round to nearest even).  The pass takes this hop as a packed
+    binary16 add; a NaN sum must give a NaN."""
+    M = 1 << 28
+    N = 3 * M
+    bufs = [torch.zeros(N, dtype=torch.int16, device=DEV) for _ in range(3)]
+    bufs[2].fill_(-0x8000)                                   # binary16 -0
+    lo = torch.arange(M, dtype=torch.int32, device=DEV)
+
+    def as16(v):
+        return torch.where(v >= 0x8000, v - 0x10000, v).to(torch.int16)
+
+    with ddl.Plan(3, N, "f16", "ring") as plan:
+        for k in range(16):                                  # 2^28 pairs per pass, 2^32 in all
+            a = as16(lo & 0xFFFF)
+            b = as16((lo >> 16) + k * (M >> 16))
+            bufs[0][:M] = a
+            bufs[0][M:] = 0
+            bufs[1][:M] = b
+            bufs[1][M:] = 0
+            bufs[2].fill_(-0x8000)
+            plan.allreduce([t.view(torch.float16) for t in bufs], 1.0)
+            want = (a.view(torch.float16).float() + b.view(torch.float16).float()).half()
+            nan = torch.isnan(want)
+            for r in range(3):
+                got = bufs[r][:M]
+                assert torch.equal(got[~nan], want.view(torch.int16)[~nan]), (k, r)
+                assert bool(torch.isnan(got.view(torch.float16)[nan]).all()), (k, r)
+        plan.check()
+
+
 SLAB_CASES = [
     dict(P=4, N=50_003),
     dict(P=16, N=99_999, topo="torus", X=4, Y=4),
