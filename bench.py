@@ -44,6 +44,7 @@ NCU_TRAFFIC = {
     ("torus4x4_resnet50", "ldg", "0e52a75d29912526"): 1_635_956_224 + 1_575_996_160,
     ("torus4x4_resnet50", "ldg", "114f33c52577cd67"): 1_635_897_344 + 1_575_593_472,
     ("torus4x4_resnet50", "ldg", "316feed84c50fe44"): 1_636_111_360 + 1_575_655_424,
+    ("torus4x4_resnet50", "ldg", "2e312619baf89fcd"): 1_636_190_976 + 1_575_729_664,
 }
 
 KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]
@@ -55,6 +56,59 @@ def kernel_hash() -> str:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def host_link_study(host, bufs, stream, dev, reps: int = 3) -> dict:
+    """Plain copies between the same page-locked host buffers and device
+    buffers: the ceiling of the end-to-end paths.  `both_gbs` moves every rank
+    in and every rank out with the two directions running at once (half of the
+    ranks each way per phase, on two streams), in the e2e formula's units."""
+    import torch
+    P = len(host)
+    nbytes = sum(h.numel() * h.element_size() for h in host)
+    side = torch.cuda.Stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def h2d(ranks, st):
+        with torch.cuda.stream(st):
+            for r in ranks:
+                bufs[r].copy_(host[r], non_blocking=True)
+
+    def d2h(ranks, st):
+        with torch.cuda.stream(st):
+            for r in ranks:
+                host[r].copy_(bufs[r], non_blocking=True)
+
+    def both():
+        lo, hi = range(P // 2), range(P // 2, P)
+        side.wait_stream(stream)
+        h2d(lo, stream)
+        d2h(hi, side)
+        stream.wait_stream(side)
+        side.wait_stream(stream)
+        h2d(hi, stream)
+        d2h(lo, side)
+        stream.wait_stream(side)
+
+    def best_ms(fn):
+        out = None
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            ev[0].record(stream)
+            fn()
+            ev[1].record(stream)
+            torch.cuda.synchronize(dev)
+            t = ev[0].elapsed_time(ev[1])
+            out = t if out is None else min(out, t)
+        return out
+
+    t_in = best_ms(lambda: h2d(range(P), stream))
+    t_out = best_ms(lambda: d2h(range(P), stream))
+    t_both = best_ms(both)
+    return {"h2d_gbs": round(nbytes / t_in / 1e6, 1), "d2h_gbs": round(nbytes / t_out / 1e6, 1),
+            "both_gbs": round(2 * nbytes / t_both / 1e6, 1),
+            "method": f"torch copies, page-locked host <-> device, best of {reps}; both = all ranks in and out, "
+                      "the two directions concurrent on two streams"}
 
 
 def schedule_name(w) -> str:
@@ -516,6 +570,9 @@ def main():
                         "host buffers over the host link"}
         e2e, alt = (zero, staged) if zc_ms < e2e_ms else (staged, zero)
         e2e = dict(e2e, other_path=alt)
+        link = host_link_study(host, bufs, stream, dev)
+        link["e2e_frac_of_both"] = round(e2e["value"] / ws / link["both_gbs"], 4)
+        e2e["host_link"] = link
         del host
 
     overlap = None

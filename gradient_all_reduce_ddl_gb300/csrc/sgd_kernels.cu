@@ -82,6 +82,35 @@ __device__ __forceinline__ void fold_step(float* in, float* out, const float* v,
   }
 }
 
+// A fold position before the last with binary16 hops: every add is rounded to
+// binary16, and fl16(fl32(a + b)) is the correctly rounded binary16 sum
+// (binary32 has 24 >= 2*11 + 2 significand bits: Figueroa, "When is double
+// rounding innocuous?", 1995), so one packed add.rn.f16x2 does two lanes.
+__device__ __forceinline__ uint32_t hadd2_rn(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ void fold_step_h2(uint32_t* in, uint32_t* out, const uint4 v, int h, int g, int inner) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t a = w[i];
+    if (h != 0) a = hadd2_rn(in[i], a);
+    in[i] = a;
+    if (h == inner - 1) out[i] = g == 0 ? a : hadd2_rn(out[i], a);
+  }
+}
+
+__device__ __forceinline__ void widen_h2(const uint32_t* hv, float* f) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __half2float(__ushort_as_half((unsigned short)(hv[i] & 0xFFFFu)));
+    f[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(hv[i] >> 16)));
+  }
+}
+
 // the update of one element of one rank; returns the new parameter, writes v
 __device__ __forceinline__ float sgd_one(float g, float pv, float* mv, const SgdParams& p) {
   const float d = __fadd_rn(g, __fmul_rn(p.wd, pv));
@@ -117,8 +146,10 @@ __device__ void sgd_scalar(const SgdParams& p, char* const* gp, float* const* pp
   }
 }
 
-template <bool F16>
+// H2: binary16 with rounded hops, folded as packed pairs up to the last position
+template <bool F16, bool H2>
 __global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_constant__ SgdParams p) {
+  static_assert(F16 || !H2, "packed hops are binary16 only");
   constexpr int L = F16 ? 8 : 4;  // gradient elements per 16-byte column
   constexpr int Q = L / 4;        // 16-byte binary32 vectors per column of parameters
   __shared__ char* s_g[kMaxPSgd];
@@ -155,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_cons
     live[u] = col[u] < ve;
   }
   float in[kV][L], out[kV][L];
+  uint32_t hin[kV][4] = {}, hout[kV][4] = {};  // packed accumulators (H2)
   int h = 0, g = 0;
   for (int t0 = 0; t0 < P; t0 += kB) {
     uint4 raw[kB][kV];
@@ -170,6 +202,14 @@ __global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_cons
       if (t0 + j < P) {
 #pragma unroll
         for (int u = 0; u < kV; ++u) {
+          if constexpr (H2) {
+            if (t0 + j < P - 1) {
+              fold_step_h2(hin[u], hout[u], raw[j][u], h, g, inner);
+              continue;
+            }
+            widen_h2(hin[u], in[u]);  // the last position: its final add stays binary32
+            widen_h2(hout[u], out[u]);
+          }
           float f[L];
           unpack<F16>(raw[j][u], f);
           fold_step<L>(in[u], out[u], f, t0 + j, h, g, inner, groups, P, rh);
@@ -236,8 +276,9 @@ __global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_cons
 
 cudaError_t launch_sgd(const SgdParams& p, uint32_t n_items, bool f16, cudaStream_t stream) {
   if (n_items == 0) return cudaSuccess;
-  if (f16) fold_sgd_kernel<true><<<n_items, kThreads, 0, stream>>>(p);
-  else fold_sgd_kernel<false><<<n_items, kThreads, 0, stream>>>(p);
+  if (f16 && p.round_hops) fold_sgd_kernel<true, true><<<n_items, kThreads, 0, stream>>>(p);
+  else if (f16) fold_sgd_kernel<true, false><<<n_items, kThreads, 0, stream>>>(p);
+  else fold_sgd_kernel<false, false><<<n_items, kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
