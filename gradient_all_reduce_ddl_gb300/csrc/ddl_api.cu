@@ -206,8 +206,10 @@ ddl_status_t check_bufs(ddl_plan* p, void* const* bufs, bool device_check, bool*
 }
 
 // Fused pass over items [ia, ib): a whole bucket, or a tile-aligned element range of one.
+// early: launch as a programmatic dependent of the kernel before it on s (only
+// where nothing but that kernel orders the launch: no event waits, no copies).
 ddl_status_t run_items(ddl_plan* p, uint32_t ia, uint32_t ib, void* const* bufs, bool aligned, float scale,
-                       cudaStream_t s) {
+                       cudaStream_t s, bool early = false) {
   if (ib <= ia) return DDL_OK;
   const bool f16 = p->spec.esize == 2;
   ddl::FoldParams fp;
@@ -232,7 +234,7 @@ ddl_status_t run_items(ddl_plan* p, uint32_t ia, uint32_t ib, void* const* bufs,
   fp.n_items = ib - ia;
   fp.tile_bytes = p->spec.tile_bytes;
   set_levels(p, &fp);
-  const cudaError_t e = ddl::launch_fold(fp, ib - ia, f16, variant, s);
+  const cudaError_t e = ddl::launch_fold(fp, ib - ia, f16, variant, s, early);
   if (e != cudaSuccess) return cuda_status(e);
   ++p->launches;
   return DDL_OK;
@@ -250,7 +252,8 @@ struct BucketRange {
   ~BucketRange() { nvtxRangePop(); }
 };
 
-ddl_status_t run_bucket(ddl_plan* p, int b, void* const* bufs, bool aligned, float scale, cudaStream_t s) {
+ddl_status_t run_bucket(ddl_plan* p, int b, void* const* bufs, bool aligned, float scale, cudaStream_t s,
+                        bool early = false) {
   const ddl::Bucket& bk = p->tab.buckets[b];
   const BucketRange range(b, bk);
   const bool f16 = p->spec.esize == 2;
@@ -272,7 +275,7 @@ ddl_status_t run_bucket(ddl_plan* p, int b, void* const* bufs, bool aligned, flo
     }
     return DDL_OK;
   }
-  return run_items(p, bk.item_begin, bk.item_end, bufs, aligned, scale, s);
+  return run_items(p, bk.item_begin, bk.item_end, bufs, aligned, scale, s, early);
 }
 
 // First item of bucket b that starts at or after element x.
@@ -415,12 +418,12 @@ ddl_status_t ddl_allreduce(ddl_plan_t p, void* const* bufs, float scale, void* s
     // every bucket back to back: one launch over all work items (stored
     // bucket by bucket, so bucket 0's CTAs still start first)
     nvtxRangePushA("ddl all buckets");
-    st = run_items(p, 0, (uint32_t)p->tab.items.size(), bufs, aligned, scale, s);
+    st = run_items(p, 0, (uint32_t)p->tab.items.size(), bufs, aligned, scale, s, true);
     nvtxRangePop();
     return st;
   }
   for (int b = 0; b < (int)p->tab.buckets.size(); ++b) {
-    st = run_bucket(p, b, bufs, aligned, scale, s);
+    st = run_bucket(p, b, bufs, aligned, scale, s, true);
     if (st != DDL_OK) return st;
   }
   return DDL_OK;

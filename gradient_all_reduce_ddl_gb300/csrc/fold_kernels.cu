@@ -176,6 +176,14 @@ __device__ void fold_scalar(char* const* ptr, uint64_t e, int P, int inner, int 
   for (int t = 0; t < P; ++t) store_elem<F16>(ptr[t], e, r);
 }
 
+// Programmatic dependent launch.  The register passes let the next kernel on
+// the stream start as soon as all of their CTAs are running, and wait for the
+// kernel before them (completed, its writes visible) only after reading the
+// plan's tables, which no kernel writes.  Both are no-ops in a launch that
+// did not ask for it.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Prologue shared by the fused kernels: every thread reads the item (one
 // broadcast load), P threads read its rank order and lay the rank pointers out
 // in fold order in shared memory; one barrier.  Returns false (after setting
@@ -219,7 +227,9 @@ __global__ void __launch_bounds__(kThreads, MINB) fold_ldg_kernel(const __grid_c
   constexpr int L = F16 ? 8 : 4;  // elements per 16-byte column
   __shared__ char* s_ptr[kMaxP];
   Item s_item;
+  griddep_launch_dependents();
   if (!load_item(p, s_ptr, &s_item)) return;
+  griddep_wait();
 
   const int P = p.P, inner = p.inner, groups = p.groups;
   const bool rh = F16 && p.round_hops;
@@ -371,7 +381,9 @@ __global__ void __launch_bounds__(kThreads, 2) fold_nd_kernel(const __grid_const
   constexpr int L = F16 ? 8 : 4;
   __shared__ char* s_ptr[kMaxP];
   Item s_item;
+  griddep_launch_dependents();
   if (!load_item(p, s_ptr, &s_item)) return;
+  griddep_wait();
   const int P = p.P;
   const bool rh = F16 && p.round_hops;
   const uint64_t eb = s_item.begin, ee = eb + s_item.len;
@@ -935,17 +947,31 @@ cudaError_t launch_bulk(const FoldParams& p, uint32_t n_items, cudaStream_t stre
   return cudaGetLastError();
 }
 
+// One CTA of kThreads per work item, optionally as a programmatic dependent.
+cudaError_t launch_items(void (*kernel)(FoldParams), const FoldParams& p, uint32_t n_items, cudaStream_t stream,
+                         bool early) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_items);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = early ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 template <bool F16>
-cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t stream) {
+cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t stream, bool early) {
   if constexpr (F16) {
     if (p.round_hops)
-      fold_ldg_kernel<true, true, 2, DDL_LDG_F16_B, DDL_LDG_MINB><<<n_items, kThreads, 0, stream>>>(p);
-    else
-      fold_ldg_kernel<true, false, 2, DDL_LDG_F16_B, DDL_LDG_MINB><<<n_items, kThreads, 0, stream>>>(p);
+      return launch_items(fold_ldg_kernel<true, true, 2, DDL_LDG_F16_B, DDL_LDG_MINB>, p, n_items, stream, early);
+    return launch_items(fold_ldg_kernel<true, false, 2, DDL_LDG_F16_B, DDL_LDG_MINB>, p, n_items, stream, early);
   } else {
-    fold_ldg_kernel<false, false, 2, DDL_LDG_F32_B, DDL_LDG_MINB><<<n_items, kThreads, 0, stream>>>(p);
+    return launch_items(fold_ldg_kernel<false, false, 2, DDL_LDG_F32_B, DDL_LDG_MINB>, p, n_items, stream, early);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace
@@ -961,19 +987,19 @@ cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaS
   return cudaGetLastError();
 }
 
-cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream) {
+cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream,
+                        bool early_launch) {
   if (n_items == 0) return cudaSuccess;
   if (p.nlev > 0) {  // n-D torus: the level-cascade register pass
     // fp32: two columns per thread (items up to 8 KB); fp16: one (up to 4 KB)
-    if (f16) fold_nd_kernel<true, 1, 8><<<n_items, kThreads, 0, stream>>>(p);
-    else fold_nd_kernel<false, 2, 8><<<n_items, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    if (f16) return launch_items(fold_nd_kernel<true, 1, 8>, p, n_items, stream, early_launch);
+    return launch_items(fold_nd_kernel<false, 2, 8>, p, n_items, stream, early_launch);
   }
   if (variant == kVarBulk)
     return f16 ? launch_bulk<true, true>(p, n_items, stream) : launch_bulk<false, true>(p, n_items, stream);
   if (variant == kVarBulkLoad)
     return f16 ? launch_bulk<true, false>(p, n_items, stream) : launch_bulk<false, false>(p, n_items, stream);
-  return f16 ? launch_ldg<true>(p, n_items, stream) : launch_ldg<false>(p, n_items, stream);
+  return f16 ? launch_ldg<true>(p, n_items, stream, early_launch) : launch_ldg<false>(p, n_items, stream, early_launch);
 }
 
 }  // namespace ddl

@@ -86,7 +86,11 @@ enum FoldVariant : int { kVarLdg = 1, kVarBulk = 2, kVarBulkLoad = 3 };
 cudaError_t launch_fold_tma(const FoldParams& p, const CUtensorMap& tmap, uint32_t n_items, bool f16,
                             cudaStream_t stream);
 
-cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream);
+// early_launch: launch the register passes as programmatic dependents of the
+// kernel before them on the stream (they read only the plan's tables before
+// griddepcontrol.wait, so their prologue overlaps that kernel's tail).
+cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream,
+                        bool early_launch = false);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, uint32_t n_xfers, uint64_t max_len, bool f16, cudaStream_t stream);
 
