@@ -330,6 +330,56 @@ def test_device_generator_matches_host(ddl):
             assert np.array_equal(to_numpy_bits(dev[r]), w.rank_values(r)), (dist, dtype, r)
 
 
+# The largest P the plan takes (256: rank orders are stored as bytes) on every
+# schedule, and the smallest buffers (fewer elements than ranks or chunks).
+EXTREME = [
+    dict(P=256, N=9_001),
+    dict(P=256, N=20_011, topo="multiring", k=4),
+    dict(P=256, N=12_345, topo="torus", X=16, Y=16),
+    dict(P=256, N=7_777, topo="torus_nd", dims=[4, 4, 4, 4]),
+    dict(P=5, N=1),
+    dict(P=9, N=4, topo="torus", X=3, Y=3),
+    dict(P=16, N=3, topo="multiring", k=2),
+    dict(P=8, N=5, topo="torus_nd", dims=[2, 2, 2]),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("case", EXTREME, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_extreme_shapes_match_oracle(ddl, case, dtype):
+    _check_exact(ddl, _w(dtype=dtype, **case))
+
+
+def test_more_than_2_32_elements_per_rank_sampled(ddl):
+    """Element indices past 2^32: a 3-rank fp16 ring of 2^32 + 12,345 elements
+    per rank (8.6 GB each) in 3 GiB buckets, so bucket and chunk edges and
+    work-item starts lie above 2^32.  Sampled against the oracle's closed
+    form (random, at every edge, and around 2^31 and 2^32); ranks identical."""
+    w = _w(P=3, N=(1 << 32) + 12_345, dtype="f16", bucket_bytes=3 << 30)
+    free, _ = torch.cuda.mem_get_info()
+    if free < 3 * w.N * 2 + (4 << 30):
+        pytest.skip("needs about 30 GB of free device memory")
+    bufs = device_bufs_generated(w, DEV)
+    with ddl.Plan.for_workload(w) as plan:
+        assert plan.num_buckets == 3
+        plan.allreduce(bufs, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    for r in range(1, w.P):
+        assert torch.equal(bufs[r].view(torch.int16), bufs[0].view(torch.int16)), r
+    rng = np.random.default_rng(32)
+    near = np.concatenate([np.arange(b - 40, b + 40) for b in ((1 << 31), (1 << 32), w.N - 40)])
+    idx = np.unique(np.concatenate([rng.integers(0, w.N, 60_000), edge_samples(w), near]))
+    idx = idx[(idx >= 0) & (idx < w.N)]
+    x_rows = np.stack([w.rank_values(r, idx.astype(np.uint64)) for r in range(w.P)], axis=1)
+    want = oracle.closed_form(oracle_cfg(w), x_rows, idx.astype(np.uint64), w.scale)
+    got = to_numpy_bits(bufs[0][torch.from_numpy(idx).to(DEV)])
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"{bad.size} of {idx.size} sampled elements differ, e.g. idx {idx[bad[:5]]}"
+    del bufs
+    torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------------------
 # Full-size workloads, in the configuration the bench times: every rank's
 # buffer compared on sampled elements (random and at every chunk edge) with
