@@ -55,13 +55,18 @@ struct ddl_plan {
   // host-buffer pipeline: copy-in, compute and copy-out streams, events
   cudaStream_t hs[3] = {nullptr, nullptr, nullptr};
   std::vector<cudaEvent_t> hev;
+  // the zero-copy pass's own work items (staged-size tiles), built on first use
+  ddl_plan* zc = nullptr;
 };
 
 namespace {
 
 using ddl::Spec;
 
+void drop_zero_copy(ddl_plan* p);
+
 ddl_status_t rebuild(ddl_plan* p) {
+  drop_zero_copy(p);
   ddl::Tables t;
   if (!ddl::build_tables(p->spec, p->spec.mode == ddl::kStepwise, &t)) return DDL_ERR_OOM;
   if (t.items.size() > 0xFFFFFFFFull || t.xfers.size() > 0xFFFFFFFFull) return DDL_ERR_UNSUPPORTED;
@@ -79,6 +84,17 @@ void free_device_tables(ddl_plan* p) {
   p->d_segs = nullptr;
   p->d_orders = nullptr;
   p->d_xfers = nullptr;
+}
+
+// The zero-copy helper shares its parent's device and error word; it owns
+// only its tables and per-bucket events.
+void drop_zero_copy(ddl_plan* p) {
+  ddl_plan* z = p->zc;
+  if (!z) return;
+  p->zc = nullptr;
+  free_device_tables(z);
+  for (cudaEvent_t ev : z->ev_ready) cudaEventDestroy(ev);
+  delete z;
 }
 
 template <typename T>
@@ -589,6 +605,30 @@ ddl_status_t ddl_allreduce_bucket(ddl_plan_t p, int bucket, void* const* bufs, f
 // Zero-copy form: the fused pass works on host buffers that the GPU can
 // reach directly (page-locked, managed, or pageable where the system gives
 // the GPU coherent access to it).
+// The zero-copy pass's plan: the same schedule with staged-size work items
+// for the bulk-load pass, built on the first zero-copy call; it shares the
+// parent's device and error word.
+static ddl_status_t zero_copy_plan(ddl_plan* p, ddl_plan** out) {
+  if (!p->zc) {
+    ddl_plan* z = new (std::nothrow) ddl_plan;
+    if (!z) return DDL_ERR_OOM;
+    z->spec = p->spec;
+    z->spec.tile_bytes = choose_tile(p->spec, DDL_KERNEL_BULK_LOAD);
+    z->kernel = DDL_KERNEL_BULK_LOAD;
+    z->device = p->device;
+    z->d_err = p->d_err;
+    p->zc = z;
+    ddl_status_t st = rebuild(z);
+    if (st == DDL_OK) st = ensure_device(z);
+    if (st != DDL_OK) {
+      drop_zero_copy(p);
+      return st;
+    }
+  }
+  *out = p->zc;
+  return DDL_OK;
+}
+
 static ddl_status_t allreduce_in_host_memory(ddl_plan* p, void* const* host_bufs, float scale, cudaStream_t s) {
   bool al = false;
   ddl_status_t st = check_bufs(p, host_bufs, false, &al);
@@ -597,6 +637,7 @@ static ddl_status_t allreduce_in_host_memory(ddl_plan* p, void* const* host_bufs
   if (st != DDL_OK) return st;
   int pageable = 0;
   cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, p->device);
+  bool locked = true;  // every buffer page-locked (mapped like device memory)
   for (int r = 0; r < p->spec.P; ++r) {
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, host_bufs[r]) != cudaSuccess) {
@@ -606,8 +647,24 @@ static ddl_status_t allreduce_in_host_memory(ddl_plan* p, void* const* host_bufs
     const bool reach = at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeManaged ||
                        (at.type == cudaMemoryTypeUnregistered && pageable);
     if (!reach) return DDL_ERR_INVALID_ARG;
+    locked = locked && at.type == cudaMemoryTypeHost;
   }
   if (p->spec.mode == ddl::kStepwise) return DDL_ERR_UNSUPPORTED;
+  // With the default kernel choice, aligned page-locked buffers take the
+  // bulk-load pass: its cp.async.bulk copies of whole tiles move more over the
+  // host link than the register pass's 16-byte loads.  (Up to P = 64, where
+  // its shared-memory ring still holds 1 KB per rank; the n-D torus keeps its
+  // cascade pass; managed and pageable memory keep the register pass.)
+  if (al && locked && p->kernel == DDL_KERNEL_AUTO && p->spec.mode == ddl::kFused &&
+      p->spec.topo != ddl::kTorusND && p->spec.P <= 64) {
+    ddl_plan* z = nullptr;
+    st = zero_copy_plan(p, &z);
+    if (st != DDL_OK) return st;
+    const uint64_t before = z->launches;
+    for (int b = 0; b < (int)z->tab.buckets.size() && st == DDL_OK; ++b) st = run_bucket(z, b, host_bufs, al, scale, s);
+    p->launches += z->launches - before;
+    return st;
+  }
   for (int b = 0; b < (int)p->tab.buckets.size(); ++b) {
     st = run_bucket(p, b, host_bufs, al, scale, s);
     if (st != DDL_OK) return st;
@@ -816,6 +873,7 @@ ddl_status_t ddl_plan_destroy(ddl_plan_t p) {
     cudaGetDevice(&cur);
     if (cur != p->device) cudaSetDevice(p->device);
     if (p->side) cudaStreamSynchronize(p->side);
+    drop_zero_copy(p);
     free_device_tables(p);
     cudaFree(p->d_err);
     for (int i = 0; i < 3; ++i)

@@ -210,7 +210,12 @@ ddl_status_t ddl_allreduce_bucket(ddl_plan_t plan, int bucket, void* const* rank
  *    reach: page-locked (cudaHostAlloc / cudaHostRegister), managed, or
  *    pageable on systems with coherent GPU access to pageable memory; other
  *    memory returns DDL_ERR_INVALID_ARG.  Not available in stepwise mode
- *    (DDL_ERR_UNSUPPORTED). */
+ *    (DDL_ERR_UNSUPPORTED).  With DDL_KERNEL_AUTO, P <= 64, and 16-byte
+ *    aligned page-locked buffers (not the n-D torus), the pass is the
+ *    bulk-load staged pass over a second set of work items sized for it:
+ *    its whole-tile copies move more over the host link.  The first such
+ *    call builds and uploads those items (an allocation); later calls reuse
+ *    them until the plan changes.  Results are the same bits either way. */
 ddl_status_t ddl_allreduce_host(ddl_plan_t plan, void* const* host_bufs, void* const* dev_bufs, float scale,
                                 void* stream);
 

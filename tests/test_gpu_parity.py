@@ -493,23 +493,39 @@ def test_allreduce_host_pipelined(ddl, case):
         assert np.array_equal(got, ref[r]), r
 
 
+ZERO_COPY = [
+    dict(P=8, N=400_003, topo="torus", X=4, Y=2),
+    dict(P=16, N=300_001, topo="multiring", k=2, bucket_bytes=400_000),
+    dict(P=64, N=100_003),
+    dict(P=65, N=50_001),
+]
+
+
+@pytest.mark.parametrize("kernel", ["auto", "ldg"])
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
-def test_allreduce_host_zero_copy(ddl, dtype):
-    """dev_bufs = NULL: the fused pass works on page-locked host memory in place."""
-    w = _w(P=8, N=400_003, dtype=dtype, topo="torus", X=4, Y=2, seed=31)
+@pytest.mark.parametrize("case", ZERO_COPY, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_allreduce_host_zero_copy(ddl, case, dtype, kernel):
+    """dev_bufs = NULL: the fused pass works on page-locked host memory in
+    place (by default through the bulk-load pass over its own work items, up
+    to P = 64; the register pass with kernel "ldg" or beyond P = 64); twice, so
+    the second call reuses the zero-copy tables."""
+    w = _w(dtype=dtype, seed=31, **case)
     host = _host_inputs(w)
     ref = [h.copy() for h in host]
     oracle.emulate(oracle_cfg(w), ref, w.scale)
+    ref2 = [h.copy() for h in ref]
+    oracle.emulate(oracle_cfg(w), ref2, w.scale)
     pinned = [torch.from_numpy(h.view(np.int16) if w.dtype == "f16" else h.copy()).clone().pin_memory()
               for h in host]
-    with ddl.Plan.for_workload(w) as plan:
-        plan.allreduce_host(pinned, None, w.scale)
-        torch.cuda.synchronize()
-        plan.check()
-        for r in range(w.P):
-            got = pinned[r].numpy()
-            got = got.view(np.uint16) if w.dtype == "f16" else got
-            assert np.array_equal(got, ref[r]), r
+    with ddl.Plan.for_workload(w, kernel=kernel) as plan:
+        for want in (ref, ref2):
+            plan.allreduce_host(pinned, None, w.scale)
+            torch.cuda.synchronize()
+            plan.check()
+            for r in range(w.P):
+                got = pinned[r].numpy()
+                got = got.view(np.uint16) if w.dtype == "f16" else got
+                assert np.array_equal(got, want[r]), r
         # memory the GPU cannot reach is refused, unless the system gives it coherent access
         plain = [np.zeros(w.N, dtype=np.float32 if dtype == "f32" else np.uint16) for _ in range(w.P)]
         try:
