@@ -21,6 +21,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kV = 2;  // 16-byte gradient columns per thread
 constexpr int kB = 8;  // ranks' loads in flight
+#ifndef DDL_SGD_F16_UB
+#define DDL_SGD_F16_UB 1  // fp16: ranks whose parameters and momenta are loaded at once
+#endif
 
 __device__ __forceinline__ float round_h(float x) { return __half2float(__float2half_rn(x)); }
 
@@ -155,6 +158,9 @@ __global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_cons
   __shared__ char* s_g[kMaxPSgd];
   __shared__ float* s_p[kMaxPSgd];
   __shared__ float* s_m[kMaxPSgd];
+  // a programmatic dependent of the kernel before it (see launch_sgd): tables
+  // first, then wait for that kernel before touching gradients or parameters
+  asm volatile("griddepcontrol.launch_dependents;");
   const Item s_item = p.items[p.item0 + blockIdx.x];  // one broadcast load
   const uint64_t off = (uint64_t)s_item.seg * (uint64_t)p.P;
   if (!(s_item.seg < p.n_segs && off + (uint64_t)p.P <= p.n_orders)) {
@@ -169,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_cons
     s_m[t] = p.moms[r];
   }
   __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int P = p.P, inner = p.inner, groups = p.groups;
   const bool rh = F16 && p.round_hops;
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_cons
     if (F16) unpack<F16>(res[u], gm[u]);  // the update reads the gradient as stored
   }
   // the update: parameter and momentum loads of kUB ranks in flight at once
-  constexpr int kUB = F16 ? 1 : 4;  // fp16 columns carry twice the parameters
+  constexpr int kUB = F16 ? DDL_SGD_F16_UB : 4;  // fp16 columns carry twice the parameters
   for (int t0 = 0; t0 < P; t0 += kUB) {
     float4 pw[kUB][kV][Q], mw[kUB][kV][Q];
 #pragma unroll
@@ -274,12 +281,23 @@ __global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_cons
 
 }  // namespace
 
+// One CTA per work item, launched as a programmatic dependent of the kernel
+// before it on the stream: its table prologue overlaps that kernel's tail.
 cudaError_t launch_sgd(const SgdParams& p, uint32_t n_items, bool f16, cudaStream_t stream) {
   if (n_items == 0) return cudaSuccess;
-  if (f16 && p.round_hops) fold_sgd_kernel<true, true><<<n_items, kThreads, 0, stream>>>(p);
-  else if (f16) fold_sgd_kernel<true, false><<<n_items, kThreads, 0, stream>>>(p);
-  else fold_sgd_kernel<false, false><<<n_items, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  void (*kernel)(SgdParams) = f16 && p.round_hops ? fold_sgd_kernel<true, true>
+                              : f16               ? fold_sgd_kernel<true, false>
+                                                  : fold_sgd_kernel<false, false>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_items);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace ddl
