@@ -117,6 +117,8 @@ def schedule_name(w) -> str:
         return f"torus {w.X}x{w.Y}"
     if w.topo == "multiring":
         return f"multi-ring k={w.k}"
+    if w.topo == "torus_nd":
+        return "torus " + "x".join(str(d) for d in w.dims)
     return "ring"
 
 

@@ -144,7 +144,8 @@ void set_levels(const ddl_plan* p, ddl::FoldParams* fp) {
 uint32_t choose_tile(const Spec& s, int kernel) {
   const uint32_t ldg = ddl::ldg_tile_bytes(s.N * (uint64_t)s.esize);
   if (s.topo == ddl::kTorusND) {
-    const uint32_t cap = s.esize == 2 ? 4096u : 8192u;  // the n-D pass's columns per thread
+    // the n-D pass's columns per thread: two, except fp16 without rounded hops
+    const uint32_t cap = (s.esize == 2 && s.mode != ddl::kFused) ? 4096u : 8192u;
     return ldg < cap ? ldg : cap;
   }
   if (kernel == DDL_KERNEL_BULK || kernel == DDL_KERNEL_BULK_LOAD || kernel == DDL_KERNEL_TMA)

@@ -363,6 +363,73 @@ struct Cascade {
   }
 };
 
+// The same cascade on binary16 pairs with rounded hops, for V columns (one
+// set of group counters: every column of a thread follows the same order).
+// Every position but the last adds packed (hadd2_rn, the rounded binary32 add
+// bit for bit).  At the last position every group closes: the adds below
+// level `top` are rounded as before, and the add at level `top` is the final
+// one, taken in binary32; levels above `top` have size 1.
+template <int V>
+struct CascadeH2 {
+  uint32_t a0[V][4], a1[V][4], a2[V][4], a3[V][4];
+  int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+
+  __device__ __forceinline__ static void add(uint32_t (*acc)[4], const uint32_t (*cur)[4], bool first) {
+#pragma unroll
+    for (int u = 0; u < V; ++u)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[u][i] = first ? cur[u][i] : hadd2_rn(acc[u][i], cur[u][i]);
+  }
+  // a position before the last
+  __device__ __forceinline__ void push(const uint32_t (*v)[4], const FoldParams& p) {
+    add(a0, v, c0 == 0);
+    if (++c0 < (int)p.lev[0]) return;
+    c0 = 0;
+    if (p.nlev < 2) return;
+    add(a1, a0, c1 == 0);
+    if (++c1 < (int)p.lev[1]) return;
+    c1 = 0;
+    if (p.nlev < 3) return;
+    add(a2, a1, c2 == 0);
+    if (++c2 < (int)p.lev[2]) return;
+    c2 = 0;
+    if (p.nlev < 4) return;
+    add(a3, a2, c3 == 0);
+    if (++c3 < (int)p.lev[3]) return;
+    c3 = 0;
+  }
+  // the top level's add: binary32, unrounded
+  __device__ __forceinline__ static void at_top(const uint32_t (*acc)[4], bool first, const uint32_t (*x)[4],
+                                                float (*out)[8]) {
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      widen_h2(x[u], out[u]);
+      if (first) continue;
+      float a[8];
+      widen_h2(acc[u], a);
+#pragma unroll
+      for (int l = 0; l < 8; ++l) out[u][l] = __fadd_rn(a[l], out[u][l]);
+    }
+  }
+  // the last position's values; writes the fold's binary32 results
+  __device__ __forceinline__ void last(uint32_t (*x)[4], const FoldParams& p, float (*out)[8]) const {
+    const int top = p.top;
+    if (top < 0) {
+#pragma unroll
+      for (int u = 0; u < V; ++u) widen_h2(x[u], out[u]);
+      return;
+    }
+    // below the top x = acc + x, rounded, unless x opens the group
+    if (top == 0) return at_top(a0, c0 == 0, x, out);
+    if (c0 != 0) add(x, a0, false);
+    if (top == 1) return at_top(a1, c1 == 0, x, out);
+    if (c1 != 0) add(x, a1, false);
+    if (top == 2) return at_top(a2, c2 == 0, x, out);
+    if (c2 != 0) add(x, a2, false);
+    at_top(a3, c3 == 0, x, out);
+  }
+};
+
 template <bool F16>
 __device__ __forceinline__ void fold_nd_scalar(const FoldParams& p, char* const* ptr, uint64_t e, bool rh) {
   Cascade<1> cs;
@@ -444,6 +511,88 @@ __global__ void __launch_bounds__(kThreads, 2) fold_nd_kernel(const __grid_const
   if (threadIdx.x < nh + nt) {
     const uint64_t e = threadIdx.x < nh ? eb + threadIdx.x : ve * L + (threadIdx.x - nh);
     fold_nd_scalar<F16>(p, s_ptr, e, rh);
+  }
+}
+
+// binary16 with rounded hops: the packed cascade; V columns per thread
+template <int V, int B>
+__global__ void __launch_bounds__(kThreads, 2) fold_nd_h2_kernel(const __grid_constant__ FoldParams p) {
+  constexpr int L = 8;
+  __shared__ char* s_ptr[kMaxP];
+  Item s_item;
+  griddep_launch_dependents();
+  if (!load_item(p, s_ptr, &s_item)) return;
+  griddep_wait();
+  const int P = p.P;
+  const uint64_t eb = s_item.begin, ee = eb + s_item.len;
+  const uint64_t vb = (eb + L - 1) / L, ve = ee / L;
+
+  if (!p.vector_ok || vb >= ve) {
+    for (uint64_t e = eb + threadIdx.x; e < ee; e += kThreads) fold_nd_scalar<true>(p, s_ptr, e, true);
+    return;
+  }
+  if (ve - vb > (uint64_t)V * kThreads) {  // V columns per thread cover the largest item
+    if (threadIdx.x == 0) atomicOr(p.err, kErrBadItem);
+    return;
+  }
+  uint64_t col[V];
+  bool live[V];
+#pragma unroll
+  for (int u = 0; u < V; ++u) {
+    col[u] = vb + threadIdx.x + (uint64_t)u * kThreads;
+    live[u] = col[u] < ve;
+  }
+  CascadeH2<V> cs;
+  uint32_t xl[V][4];  // the last position's values
+  for (int t0 = 0; t0 < P; t0 += B) {
+    uint4 raw[B][V];
+#pragma unroll
+    for (int j = 0; j < B; ++j)
+      if (t0 + j < P) {
+#pragma unroll
+        for (int u = 0; u < V; ++u)
+          raw[j][u] = live[u] ? __ldcs(reinterpret_cast<const uint4*>(s_ptr[t0 + j]) + col[u]) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+    for (int j = 0; j < B; ++j) {
+      if (t0 + j < P) {
+        uint32_t w[V][4];
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          w[u][0] = raw[j][u].x;
+          w[u][1] = raw[j][u].y;
+          w[u][2] = raw[j][u].z;
+          w[u][3] = raw[j][u].w;
+        }
+        if (t0 + j < P - 1) {
+          cs.push(w, p);
+        } else {
+#pragma unroll
+          for (int u = 0; u < V; ++u)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xl[u][i] = w[u][i];
+        }
+      }
+    }
+  }
+  float fin[V][L];
+  cs.last(xl, p, fin);
+  uint4 res[V];
+#pragma unroll
+  for (int u = 0; u < V; ++u) {
+#pragma unroll
+    for (int l = 0; l < L; ++l) fin[u][l] = __fmul_rn(fin[u][l], p.scale);
+    res[u] = pack<true>(fin[u]);
+  }
+  for (int t = 0; t < P; ++t) {
+#pragma unroll
+    for (int u = 0; u < V; ++u)
+      if (live[u]) __stcs(reinterpret_cast<uint4*>(s_ptr[t]) + col[u], res[u]);
+  }
+  const uint64_t nh = vb * L - eb, nt = ee - ve * L;
+  if (threadIdx.x < nh + nt) {
+    const uint64_t e = threadIdx.x < nh ? eb + threadIdx.x : ve * L + (threadIdx.x - nh);
+    fold_nd_scalar<true>(p, s_ptr, e, true);
   }
 }
 
@@ -991,7 +1140,9 @@ cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int var
                         bool early_launch) {
   if (n_items == 0) return cudaSuccess;
   if (p.nlev > 0) {  // n-D torus: the level-cascade register pass
-    // fp32: two columns per thread (items up to 8 KB); fp16: one (up to 4 KB)
+    // two columns per thread (items up to 8 KB); fp16 with rounded hops folds
+    // packed pairs, fp16 without them (unused by the plans) one column (4 KB)
+    if (f16 && p.round_hops) return launch_items(fold_nd_h2_kernel<2, 6>, p, n_items, stream, early_launch);
     if (f16) return launch_items(fold_nd_kernel<true, 1, 8>, p, n_items, stream, early_launch);
     return launch_items(fold_nd_kernel<false, 2, 8>, p, n_items, stream, early_launch);
   }

@@ -174,6 +174,11 @@ WORKLOADS = {
     "torus4x4x4_resnet101": Workload("torus4x4x4_resnet101", P=64, N=sum(RESNET101), dtype="f32",
                                      topo="torus_nd", dims=(4, 4, 4), bucket_bytes=25 * 2 ** 20,
                                      layers=tuple(RESNET101), scale=1.0 / 64, sigma=1e-3, seed=_SEED0 + 6),
+    # n-D torus 4x4x2 (P=32) with fp16 hops on the ResNet-50 layout: the 8x4
+    # fp16 torus's bytes on three dimensions
+    "torus4x4x2_resnet50_f16": Workload("torus4x4x2_resnet50_f16", P=32, N=sum(RESNET50), dtype="f16",
+                                        topo="torus_nd", dims=(4, 4, 2), layers=tuple(RESNET50),
+                                        scale=1.0 / 32, sigma=1e-2, seed=_SEED0 + 7),
     # P=16, 300M fp32 (1.2 GB per rank, the language model's gradient), N(0, 1e-4)
     "ring16_lm300m": Workload("ring16_lm300m", P=16, N=300_000_000, dtype="f32", topo="ring",
                               scale=1.0 / 16, sigma=1e-4, seed=_SEED0 + 5),

@@ -95,12 +95,13 @@ def test_cost_model_matches_oracle(ddl, case):
 
 
 @pytest.mark.parametrize("name", ["torus4x4_resnet50", "torus8x4_resnet50_f16", "multiring64_resnet101",
-                                  "ring16_lm300m", "torus4x4_lm300m"])
+                                  "ring16_lm300m", "torus4x4_lm300m", "torus4x4x4_resnet101",
+                                  "torus4x4x2_resnet50_f16"])
 def test_workload_tables_match_oracle(ddl, name):
     w = synth.WORKLOADS[name]
     with ddl.Plan.for_workload(w) as plan:
         cfg = oracle.Config(w.P, w.N, w.dtype, w.topo, k=w.k, X=w.X, Y=w.Y, bucket_bytes=w.bucket_bytes,
-                            layers=w.layers)
+                            layers=w.layers, dims=w.dims)
         assert plan.buckets() == oracle.buckets(cfg)
         moved, steps = plan.traffic()
         assert moved == 2 * (w.P - 1) * w.N

@@ -387,7 +387,7 @@ def test_more_than_2_32_elements_per_rank_sampled(ddl):
 # ---------------------------------------------------------------------------
 
 FULL = ["ring4_int", "torus4x4_resnet50", "torus8x4_resnet50_f16", "multiring64_resnet101", "ring16_lm300m",
-        "multiring16_lm300m", "torus4x4_lm300m", "torus4x4x4_resnet101"]
+        "multiring16_lm300m", "torus4x4_lm300m", "torus4x4x4_resnet101", "torus4x4x2_resnet50_f16"]
 
 
 @pytest.mark.parametrize("kernel", ["auto", "bulk", "bulkload"])
@@ -533,6 +533,45 @@ def test_allreduce_host_zero_copy(ddl, case, dtype, kernel):
             torch.cuda.synchronize()
         except ddl.DDLError as e:
             assert e.status == ddl.DDL_ERR_INVALID_ARG
+
+
+def test_zero_copy_tables_follow_plan_changes(ddl):
+    """The zero-copy pass's own work items are rebuilt when the plan changes:
+    zero-copy, then a layer list (new buckets), zero-copy again, then
+    rank-order mode, then stepwise (refused); each result against the oracle
+    (rank order against the fp64 sum), launches counted on the plan."""
+    w = _w(P=16, N=200_003, topo="multiring", k=2, bucket_bytes=300_000, seed=77)
+
+    def pinned_inputs(wk):
+        host = _host_inputs(wk)
+        return host, [torch.from_numpy(h.copy()).pin_memory() for h in host]
+
+    with ddl.Plan.for_workload(w) as plan:
+        w2 = w.with_(layers=(50_000, 3, 80_000, 70_000))
+        for wk in (w, w2):
+            if wk is w2:
+                ddl.ddl_plan_set_layers(plan.handle, list(wk.layers))
+            host, pinned = pinned_inputs(wk)
+            before = plan.launches
+            plan.allreduce_host(pinned, None, wk.scale)
+            torch.cuda.synchronize()
+            plan.check()
+            assert plan.launches - before == plan.num_buckets
+            ref = [h.copy() for h in host]
+            oracle.emulate(oracle_cfg(wk), ref, wk.scale)
+            for r in range(wk.P):
+                assert np.array_equal(pinned[r].numpy(), ref[r]), (wk.layers, r)
+        plan.set_mode("rankorder")
+        host, pinned = pinned_inputs(w2)
+        plan.allreduce_host(pinned, None, w2.scale)
+        torch.cuda.synchronize()
+        ref = oracle.ref64(host, w2.scale, "f32")
+        got = pinned[0].numpy().astype(np.float64)
+        assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 1e-6
+        plan.set_mode("stepwise")
+        with pytest.raises(ddl.DDLError) as ei:
+            plan.allreduce_host(pinned, None, w2.scale)
+        assert ei.value.status == ddl.DDL_ERR_UNSUPPORTED
 
 
 def test_allreduce_captured_in_cuda_graph(ddl):
