@@ -46,6 +46,7 @@ NCU_TRAFFIC = {
     ("torus4x4_resnet50", "ldg", "316feed84c50fe44"): 1_636_111_360 + 1_575_655_424,
     ("torus4x4_resnet50", "ldg", "2e312619baf89fcd"): 1_636_190_976 + 1_575_729_664,
     ("torus4x4_resnet50", "ldg", "2c4e6c02dcdb9dcd"): 1_635_898_368 + 1_576_063_744,
+    ("torus4x4_resnet50", "ldg", "8b82de61611a4d5b"): 1_635_897_088 + 1_575_497_728,
 }
 
 KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]
