@@ -522,15 +522,20 @@ def main():
                              "tma": "fold_tma_kernel" if args.slab else "fold_ldg_kernel"}.get(args.kernel,
                                                                                             "fold_ldg_kernel"),
                    "rankorder": "fold_ldg_kernel (rank order)", "stepwise": "step_kernel"}[args.mode]
+    kernel_bytes = nbytes
     if args.mode == "stepwise":
-        achieved = None
-    else:
-        achieved = nbytes / (avg_call_ms * 1e-3) / 1e9  # bytes of all buckets / time of the call
-    traffic = NCU_TRAFFIC.get((w.name, args.kernel if args.kernel != "auto" else "ldg", kernel_hash()))
+        # the step kernels' own minimum: a reduce-scatter message element reads
+        # two values and writes one, an all-gather element reads one and writes
+        # one, and each half of the 2(P-1)N elements moved is one of the two
+        moved = plan.traffic()[0]
+        kernel_bytes = (moved // 2) * 5 * w.esize if moved else 2 * w.N * w.esize
+    achieved = kernel_bytes / (avg_call_ms * 1e-3) / 1e9  # bytes of all launches / time of the call
+    traffic = (NCU_TRAFFIC.get((w.name, args.kernel if args.kernel != "auto" else "ldg", kernel_hash()))
+               if args.mode == "fused" else None)
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": None if achieved is None else round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": None if achieved is None else round(achieved / peak, 4),
                 "peak_kind": f"hbm_gbs of {peak_kind}", "traffic": traffic,
-                "algorithmic_bytes_per_launch": nbytes // max(1, launches_per_call),
+                "algorithmic_bytes_per_launch": kernel_bytes // max(1, launches_per_call),
                 "launches_per_step": launches_per_call,
                 "avg_call_ms": round(avg_call_ms, 4)}
 

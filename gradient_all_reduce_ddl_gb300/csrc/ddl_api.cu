@@ -286,7 +286,9 @@ ddl_status_t run_bucket(ddl_plan* p, int b, void* const* bufs, bool aligned, flo
     for (uint32_t st = bk.step_begin; st < bk.step_end; ++st) {
       const ddl::Step& step = p->tab.steps[st];
       sp.xfer0 = step.xfer_begin;
-      const cudaError_t e = ddl::launch_step(sp, step.xfer_end - step.xfer_begin, step.max_len, f16, s);
+      // every step after the first follows this bucket's previous step on s
+      const cudaError_t e =
+          ddl::launch_step(sp, step.xfer_end - step.xfer_begin, step.max_len, f16, s, early || st > bk.step_begin);
       if (e != cudaSuccess) return cuda_status(e);
       ++p->launches;
     }

@@ -92,6 +92,9 @@ cudaError_t launch_fold_tma(const FoldParams& p, const CUtensorMap& tmap, uint32
 cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream,
                         bool early_launch = false);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
-cudaError_t launch_step(const StepParams& p, uint32_t n_xfers, uint64_t max_len, bool f16, cudaStream_t stream);
+// early_launch: as for launch_fold (the step kernel reads only its message
+// table before griddepcontrol.wait).
+cudaError_t launch_step(const StepParams& p, uint32_t n_xfers, uint64_t max_len, bool f16, cudaStream_t stream,
+                        bool early_launch = false);
 
 }  // namespace ddl

@@ -50,15 +50,11 @@ __device__ __forceinline__ void op_elem(const Xfer& x, const char* src, char* ds
   st1<F16>(dst, e, v);
 }
 
+// One 16-byte column of a message: the receiver's value dr and the sender's sr
+// (loaded by the caller) give the value the receiver stores.
 template <bool F16>
-__device__ __forceinline__ void op_vec(const Xfer& x, const uint4* src, uint4* dst, uint64_t c, float scale) {
-  constexpr int L = F16 ? 8 : 4;
-  if (x.op == kCopy) {
-    dst[c] = src[c];
-    return;
-  }
-  const uint4 dr = dst[c];
-  const uint4 sr = (x.op == kScaleOnly) ? dr : src[c];
+__device__ __forceinline__ uint4 op_vec(const Xfer& x, const uint4 dr, const uint4 sr, float scale) {
+  if (x.op == kCopy) return sr;
   const uint32_t dw[4] = {dr.x, dr.y, dr.z, dr.w}, sw[4] = {sr.x, sr.y, sr.z, sr.w};
   uint32_t ow[4];
 #pragma unroll
@@ -81,15 +77,18 @@ __device__ __forceinline__ void op_vec(const Xfer& x, const uint4* src, uint4* d
       ow[i] = __float_as_uint(v);
     }
   }
-  (void)L;
-  dst[c] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+  return make_uint4(ow[0], ow[1], ow[2], ow[3]);
 }
 
-// grid.x: tiles of kTileBytes over the step's longest message; grid.y: message
+// grid.x: tiles of kTileBytes over the step's longest message; grid.y: message.
+// Launched as a programmatic dependent of the step before it: a CTA reads its
+// message from the plan's table, then waits for that step (finished, writes
+// visible) before touching a buffer.
 template <bool F16>
 __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ StepParams p) {
   constexpr int L = F16 ? 8 : 4;
   constexpr uint64_t kTile = (uint64_t)kTileBytes / (F16 ? 2 : 4);
+  asm volatile("griddepcontrol.launch_dependents;");
   const Xfer x = p.xfers[p.xfer0 + blockIdx.y];
   const uint64_t off = (uint64_t)blockIdx.x * kTile;
   if (off >= x.len) return;
@@ -97,6 +96,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
     if (threadIdx.x == 0) atomicOr(p.err, kErrBadXfer);
     return;
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const char* src = static_cast<const char*>(p.bufs[x.src]);
   char* dst = static_cast<char*>(p.bufs[x.dst]);
   const uint64_t eb = x.lo + off, ee = x.lo + (x.len < off + kTile ? x.len : off + kTile);
@@ -105,8 +105,19 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
     for (uint64_t e = eb + threadIdx.x; e < ee; e += kThreads) op_elem<F16>(x, src, dst, e, p.scale);
     return;
   }
-  for (uint64_t c = vb + threadIdx.x; c < ve; c += kThreads)
-    op_vec<F16>(x, reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), c, p.scale);
+  // two columns per thread per round: all four loads issued before any store
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  const bool need_dst = x.op != kCopy, need_src = x.op != kScaleOnly;
+  for (uint64_t c0 = vb + threadIdx.x; c0 < ve; c0 += 2 * kThreads) {
+    const uint64_t c1 = c0 + kThreads;
+    const bool two = c1 < ve;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    const uint4 d0 = need_dst ? d4[c0] : z, s0 = need_src ? s4[c0] : z;
+    const uint4 d1 = (two && need_dst) ? d4[c1] : z, s1 = (two && need_src) ? s4[c1] : z;
+    d4[c0] = op_vec<F16>(x, d0, need_src ? s0 : d0, p.scale);
+    if (two) d4[c1] = op_vec<F16>(x, d1, need_src ? s1 : d1, p.scale);
+  }
   const uint64_t nh = vb * L - eb, nt = ee - ve * L;
   if (threadIdx.x < nh + nt) {
     const uint64_t e = threadIdx.x < nh ? eb + threadIdx.x : ve * L + (threadIdx.x - nh);
@@ -116,13 +127,20 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
 
 }  // namespace
 
-cudaError_t launch_step(const StepParams& p, uint32_t n_xfers, uint64_t max_len, bool f16, cudaStream_t stream) {
+cudaError_t launch_step(const StepParams& p, uint32_t n_xfers, uint64_t max_len, bool f16, cudaStream_t stream,
+                        bool early_launch) {
   if (n_xfers == 0 || max_len == 0) return cudaSuccess;
   const uint64_t tile = (uint64_t)kTileBytes / (f16 ? 2 : 4);
-  const dim3 grid((unsigned)((max_len + tile - 1) / tile), n_xfers);
-  if (f16) step_kernel<true><<<grid, kThreads, 0, stream>>>(p);
-  else step_kernel<false><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((max_len + tile - 1) / tile), n_xfers);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = early_launch ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, f16 ? step_kernel<true> : step_kernel<false>, p);
 }
 
 }  // namespace ddl

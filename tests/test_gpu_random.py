@@ -1,6 +1,6 @@
 """Randomised small problems on the GPU, every schedule: the fused pass (a
-random kernel variant) and the stepwise mode must match the oracle's step
-emulation bit for bit."""
+random kernel variant), the stepwise mode and the zero-copy pass over
+page-locked host memory must match the oracle's step emulation bit for bit."""
 import numpy as np
 import pytest
 
@@ -23,7 +23,7 @@ def ddl():
     return mod
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", range(32))
 def test_random_problem_matches_oracle(ddl, seed):
     rng = np.random.default_rng(5000 + seed)
     kw = _random_problem(rng)
@@ -48,3 +48,13 @@ def test_random_problem_matches_oracle(ddl, seed):
             plan.check()
         for r in range(w.P):
             assert np.array_equal(to_numpy_bits(bufs[r]), ref[r]), (kw, mode, kernel, r)
+    pinned = [torch.from_numpy(h.view(np.int16) if w.dtype == "f16" else h.copy()).clone().pin_memory()
+              for h in host]
+    with ddl.Plan.for_workload(w) as plan:
+        plan.allreduce_host(pinned, None, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    for r in range(w.P):
+        got = pinned[r].numpy()
+        got = got.view(np.uint16) if w.dtype == "f16" else got
+        assert np.array_equal(got, ref[r]), (kw, "zero-copy", r)
