@@ -574,6 +574,43 @@ def test_zero_copy_tables_follow_plan_changes(ddl):
         assert ei.value.status == ddl.DDL_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("case", [dict(P=16, N=300_001, topo="torus", X=4, Y=4),
+                                  dict(P=8, N=200_003, topo="torus_nd", dims=[2, 2, 2], dtype="f16"),
+                                  dict(P=16, N=250_001, topo="multiring", k=2, bucket_bytes=300_000),
+                                  dict(P=6, N=100_003, topo="torus", X=3, Y=2, mode="stepwise")],
+                         ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_back_to_back_calls_and_producer_kernels(ddl, case):
+    """Passes launched as programmatic dependents must still see every write
+    of the kernel before them: three all-reduces queued back to back, with a
+    torch kernel that rewrites every rank buffer (x -> 2x - 1, exact here)
+    before the second, and no synchronisation between any of them."""
+    case = dict(case)
+    mode = case.pop("mode", "fused")
+    w = _w(seed=88, **case)
+    host = _host_inputs(w)
+    ref = [h.copy() for h in host]
+    cfg = oracle_cfg(w)
+    oracle.emulate(cfg, ref, w.scale)
+    if w.dtype == "f16":
+        ref = [oracle.f32_to_f16(2.0 * oracle.f16_to_f32(r) - 1.0) for r in ref]
+    else:
+        ref = [(np.float32(2.0) * r - np.float32(1.0)).astype(np.float32) for r in ref]
+    oracle.emulate(cfg, ref, w.scale)
+    oracle.emulate(cfg, ref, w.scale)
+    bufs = device_bufs_from_host(host, DEV)
+    torch.cuda.synchronize()
+    with ddl.Plan.for_workload(w, mode=mode) as plan:
+        plan.allreduce(bufs, w.scale)
+        for b in bufs:
+            b.mul_(2).sub_(1)
+        plan.allreduce(bufs, w.scale)
+        plan.allreduce(bufs, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    for r in range(w.P):
+        assert np.array_equal(to_numpy_bits(bufs[r]), ref[r]), r
+
+
 def test_allreduce_captured_in_cuda_graph(ddl):
     """After a first (uploading) call, ddl_allreduce can be captured in a CUDA
     graph; each replay reduces whatever the buffers hold at that time."""
