@@ -153,7 +153,11 @@ ddl_status_t ddl_plan_set_kernel(ddl_plan_t plan, ddl_kernel_t kernel);
  *    take a slower element-wise path; results do not change.
  *  scale: binary32 factor applied once per element (1/P gives the mean).
  * The first call on a device uploads the plan's tables (device memory owned
- * by the plan) and creates its side stream and events. */
+ * by the plan) and creates its side stream and events.
+ * Stream order is kept.  The launch is a programmatic dependent of the kernel
+ * before it on `stream`: its CTAs may start and read the plan's tables while
+ * that kernel drains, but touch no rank buffer until every earlier kernel on
+ * the stream has finished and its writes are visible. */
 ddl_status_t ddl_allreduce(ddl_plan_t plan, void* const* rank_bufs, float scale, void* stream);
 
 /* All-reduce followed by the synchronous-SGD update, in the same HBM pass.
