@@ -60,6 +60,22 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def sample_config(oracle, w, n: int):
+    """The oracle's configuration for the first n elements of each rank of w:
+    the same schedule (n-D dims included), bucket size, and the layer list cut
+    at n."""
+    layers = None
+    if w.layers is not None:
+        acc, layers = 0, []
+        for v in w.layers:
+            if acc >= n:
+                break
+            layers.append(min(v, n - acc))
+            acc += layers[-1]
+    return oracle.Config(w.P, n, w.dtype, w.topo, k=w.k, X=w.X, Y=w.Y, bucket_bytes=w.bucket_bytes, layers=layers,
+                         dims=w.dims)
+
+
 def host_link_study(host, bufs, stream, dev, reps: int = 3) -> dict:
     """Plain copies between the same page-locked host buffers and device
     buffers: the ceiling of the end-to-end paths.  `both_gbs` moves every rank
@@ -193,15 +209,7 @@ def cpu_baseline(w, target_s: float = 10.0, max_elems: int = 2_000_000):
     import oracle
     n = min(w.N, max_elems)
     host = [synth.draw_rank(w.seed, r, n, w.dist, w.sigma, w.dtype) for r in range(w.P)]
-    layers = None
-    if w.layers is not None:
-        acc, layers = 0, []
-        for v in w.layers:
-            if acc >= n:
-                break
-            layers.append(min(v, n - acc))
-            acc += layers[-1]
-    cfg = oracle.Config(w.P, n, w.dtype, w.topo, k=w.k, X=w.X, Y=w.Y, bucket_bytes=w.bucket_bytes, layers=layers)
+    cfg = sample_config(oracle, w, n)
     spent, reps = 0.0, 0
     while spent < target_s or reps < 1:
         bufs = [h.copy() for h in host]
@@ -370,7 +378,7 @@ def run_reference(args, w):
     n = int(budget_s / ((args.steps + args.warmup) * w.P * 8e-9))
     n = max(4096, min(n, w.N, 2_000_000))
     host = [synth.draw_rank(w.seed, r, n, w.dist, w.sigma, w.dtype) for r in range(w.P)]
-    cfg = oracle.Config(w.P, n, w.dtype, w.topo, k=w.k, X=w.X, Y=w.Y)
+    cfg = sample_config(oracle, w, n)
     times = []
     for i in range(args.warmup + args.steps):
         bufs = [h.copy() for h in host]

@@ -24,3 +24,15 @@ def test_reference_arm_json_line():
     assert d["config"]["workload"] == "ring4_int"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_reference_arm_on_an_n_d_torus_sample():
+    """The reference arm's oracle sample keeps the workload's schedule: an
+    n-D torus with layer-list buckets, cut to 20,000 elements per rank."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "torus4x4x4_resnet101", "--elems", "20000", "--steps", "2", "--warmup", "3"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([l for l in r.stdout.splitlines() if l.strip()][-1])
+    assert d["config"]["schedule"] == "torus 4x4x4" and d["value"] > 0
