@@ -714,7 +714,12 @@ ddl_status_t ddl_allreduce_host(ddl_plan_t p, void* const* host_bufs, void* cons
   // (tile-aligned, so each range is a run of whole work items) on three
   // streams: copy-in of range i+1 and copy-out of range i-1 overlap the pass
   // over range i, and the two copy directions overlap each other.
-  constexpr int kMaxRanges = 32;
+  // Eight ranges: more of them queue more copies than the streams retire in
+  // step (32 ranges of the 4x4 ResNet-50 gradient took 13.6 ms, 8 took 11.6).
+#ifndef DDL_HOST_RANGES
+#define DDL_HOST_RANGES 8
+#endif
+  constexpr int kMaxRanges = DDL_HOST_RANGES;
   const uint64_t tile = (uint64_t)p->spec.tile_bytes / es;
   uint64_t R = (p->spec.N + kMaxRanges - 1) / kMaxRanges;
   R = ((R + tile - 1) / tile) * tile;
