@@ -369,7 +369,9 @@ struct Cascade {
 // bit for bit).  At the last position every group closes: the adds below
 // level `top` are rounded as before, and the add at level `top` is the final
 // one, taken in binary32; levels above `top` have size 1.
-template <int V>
+// NL: the plan's number of levels (a compile-time count, so unused levels
+// take no registers).
+template <int V, int NL>
 struct CascadeH2 {
   uint32_t a0[V][4], a1[V][4], a2[V][4], a3[V][4];
   int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
@@ -385,18 +387,21 @@ struct CascadeH2 {
     add(a0, v, c0 == 0);
     if (++c0 < (int)p.lev[0]) return;
     c0 = 0;
-    if (p.nlev < 2) return;
-    add(a1, a0, c1 == 0);
-    if (++c1 < (int)p.lev[1]) return;
-    c1 = 0;
-    if (p.nlev < 3) return;
-    add(a2, a1, c2 == 0);
-    if (++c2 < (int)p.lev[2]) return;
-    c2 = 0;
-    if (p.nlev < 4) return;
-    add(a3, a2, c3 == 0);
-    if (++c3 < (int)p.lev[3]) return;
-    c3 = 0;
+    if constexpr (NL >= 2) {
+      add(a1, a0, c1 == 0);
+      if (++c1 < (int)p.lev[1]) return;
+      c1 = 0;
+    }
+    if constexpr (NL >= 3) {
+      add(a2, a1, c2 == 0);
+      if (++c2 < (int)p.lev[2]) return;
+      c2 = 0;
+    }
+    if constexpr (NL >= 4) {
+      add(a3, a2, c3 == 0);
+      if (++c3 < (int)p.lev[3]) return;
+      c3 = 0;
+    }
   }
   // the top level's add: binary32, unrounded
   __device__ __forceinline__ static void at_top(const uint32_t (*acc)[4], bool first, const uint32_t (*x)[4],
@@ -412,6 +417,7 @@ struct CascadeH2 {
     }
   }
   // the last position's values; writes the fold's binary32 results
+  // (top < NL: the highest level of size > 1, or -1 if there is none)
   __device__ __forceinline__ void last(uint32_t (*x)[4], const FoldParams& p, float (*out)[8]) const {
     const int top = p.top;
     if (top < 0) {
@@ -422,11 +428,15 @@ struct CascadeH2 {
     // below the top x = acc + x, rounded, unless x opens the group
     if (top == 0) return at_top(a0, c0 == 0, x, out);
     if (c0 != 0) add(x, a0, false);
-    if (top == 1) return at_top(a1, c1 == 0, x, out);
-    if (c1 != 0) add(x, a1, false);
-    if (top == 2) return at_top(a2, c2 == 0, x, out);
-    if (c2 != 0) add(x, a2, false);
-    at_top(a3, c3 == 0, x, out);
+    if constexpr (NL >= 2) {
+      if (top == 1) return at_top(a1, c1 == 0, x, out);
+      if (c1 != 0) add(x, a1, false);
+    }
+    if constexpr (NL >= 3) {
+      if (top == 2) return at_top(a2, c2 == 0, x, out);
+      if (c2 != 0) add(x, a2, false);
+    }
+    if constexpr (NL >= 4) at_top(a3, c3 == 0, x, out);
   }
 };
 
@@ -514,8 +524,19 @@ __global__ void __launch_bounds__(kThreads, 2) fold_nd_kernel(const __grid_const
   }
 }
 
-// binary16 with rounded hops: the packed cascade; V columns per thread
-template <int V, int B>
+#ifndef DDL_ND_H2_B1
+#define DDL_ND_H2_B1 8  // one or two levels
+#endif
+#ifndef DDL_ND_H2_B3
+#define DDL_ND_H2_B3 7
+#endif
+#ifndef DDL_ND_H2_B4
+#define DDL_ND_H2_B4 6
+#endif
+
+// binary16 with rounded hops: the packed cascade of NL levels; V columns per
+// thread, B ranks' loads in flight
+template <int V, int B, int NL>
 __global__ void __launch_bounds__(kThreads, 2) fold_nd_h2_kernel(const __grid_constant__ FoldParams p) {
   constexpr int L = 8;
   __shared__ char* s_ptr[kMaxP];
@@ -542,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_nd_h2_kernel(const __grid_co
     col[u] = vb + threadIdx.x + (uint64_t)u * kThreads;
     live[u] = col[u] < ve;
   }
-  CascadeH2<V> cs;
+  CascadeH2<V, NL> cs;
   uint32_t xl[V][4];  // the last position's values
   for (int t0 = 0; t0 < P; t0 += B) {
     uint4 raw[B][V];
@@ -1142,7 +1163,12 @@ cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int var
   if (p.nlev > 0) {  // n-D torus: the level-cascade register pass
     // two columns per thread (items up to 8 KB); fp16 with rounded hops folds
     // packed pairs, fp16 without them (unused by the plans) one column (4 KB)
-    if (f16 && p.round_hops) return launch_items(fold_nd_h2_kernel<2, 6>, p, n_items, stream, early_launch);
+    if (f16 && p.round_hops) {
+      if (p.nlev < 1 || p.nlev > 4) return cudaErrorInvalidValue;
+      void (*const h2[4])(FoldParams) = {fold_nd_h2_kernel<2, DDL_ND_H2_B1, 1>, fold_nd_h2_kernel<2, DDL_ND_H2_B1, 2>,
+                                         fold_nd_h2_kernel<2, DDL_ND_H2_B3, 3>, fold_nd_h2_kernel<2, DDL_ND_H2_B4, 4>};
+      return launch_items(h2[p.nlev - 1], p, n_items, stream, early_launch);
+    }
     if (f16) return launch_items(fold_nd_kernel<true, 1, 8>, p, n_items, stream, early_launch);
     return launch_items(fold_nd_kernel<false, 2, 8>, p, n_items, stream, early_launch);
   }
