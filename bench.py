@@ -410,7 +410,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--mode", default="fused", choices=["fused", "stepwise", "rankorder"])
-    ap.add_argument("--kernel", default="auto", choices=["auto", "ldg", "bulk", "bulkload", "tma"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "ldg", "bulk", "bulkload", "tma", "chunked"])
     ap.add_argument("--slab", action="store_true",
                     help="rank buffers in one slab (ddl_allreduce_slab); needed by --kernel tma")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -527,7 +527,7 @@ def main():
     # the call's average device time is this replica's timed region / steps
     avg_call_ms = local_ms / args.steps
     peak, peak_kind = measured_peak()
-    kernel_name = {"fused": {"bulk": "fold_bulk_kernel", "bulkload": "fold_bulk_kernel",
+    kernel_name = {"fused": {"bulk": "fold_bulk_kernel", "bulkload": "fold_bulk_kernel", "chunked": "fold_chunked_kernel",
                              "tma": "fold_tma_kernel" if args.slab else "fold_ldg_kernel"}.get(args.kernel,
                                                                                             "fold_ldg_kernel"),
                    "rankorder": "fold_ldg_kernel (rank order)", "stepwise": "step_kernel"}[args.mode]

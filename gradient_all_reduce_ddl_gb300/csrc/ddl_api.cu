@@ -248,6 +248,7 @@ ddl_status_t run_items(ddl_plan* p, uint32_t ia, uint32_t ib, void* const* bufs,
   int variant = ddl::kVarLdg;
   if (aligned && p->kernel == DDL_KERNEL_BULK) variant = ddl::kVarBulk;
   if (aligned && p->kernel == DDL_KERNEL_BULK_LOAD) variant = ddl::kVarBulkLoad;
+  if (aligned && p->kernel == DDL_KERNEL_CHUNKED) variant = ddl::kVarChunked;
   fp.n_items = ib - ia;
   fp.tile_bytes = p->spec.tile_bytes;
   set_levels(p, &fp);
@@ -411,7 +412,7 @@ ddl_status_t ddl_plan_set_torus_dims(ddl_plan_t p, int ndims, const int* dims) {
 }
 
 ddl_status_t ddl_plan_set_kernel(ddl_plan_t p, ddl_kernel_t k) {
-  if (!p || p->ov_active || k < DDL_KERNEL_AUTO || k > DDL_KERNEL_TMA) return DDL_ERR_INVALID_ARG;
+  if (!p || p->ov_active || k < DDL_KERNEL_AUTO || k > DDL_KERNEL_CHUNKED) return DDL_ERR_INVALID_ARG;
   const uint32_t tile = choose_tile(p->spec, (int)k);
   if (tile != p->spec.tile_bytes) {
     const Spec old = p->spec;

@@ -929,6 +929,199 @@ __global__ void __launch_bounds__(kBulkThreads, 1) fold_bulk_kernel(const __grid
 }
 
 // ---------------------------------------------------------------------------
+// Variant 5: staged through shared memory in rank chunks.  The staged
+// variants above hold all P ranks of a tile in one stage, so at large P a
+// stage carries little per rank and few consumers have work.  Here a stage
+// holds kChunk ranks (in fold order) of a whole register-pass tile (up to
+// 8 KB per rank): the producer warp streams an item's ranks through the
+// stage ring chunk by chunk with one cp.async.bulk per rank, and each of
+// the 256 consumer threads keeps its two 16-byte columns' fold in registers
+// across the item's chunks, then scales and stores the result to every rank
+// from registers.  Every wait is bounded as in the variants above.  Two
+// ranks per stage, three stages and two CTAs per SM measured fastest (8 ranks
+// per stage and one CTA: 0.92 of the copy peak at P = 16; deeper rings were
+// slower too).
+// ---------------------------------------------------------------------------
+#ifndef DDL_CHUNK_RANKS
+#define DDL_CHUNK_RANKS 2
+#endif
+#ifndef DDL_CHUNK_MINB
+#define DDL_CHUNK_MINB 2
+#endif
+#ifndef DDL_CHUNK_STAGES
+#define DDL_CHUNK_STAGES 3
+#endif
+constexpr int kChunk = DDL_CHUNK_RANKS;  // ranks per stage
+constexpr int kCStages = DDL_CHUNK_STAGES;  // depth of the stage ring
+
+struct ChunkMeta {
+  uint64_t eb, ee, vb, ve;  // item elements [eb, ee); staged columns [vb, ve)
+  uint32_t t0, nr;          // this stage's fold positions [t0, t0 + nr)
+  uint32_t ok, last;        // table entry valid; last chunk of the item
+};
+
+// stages x kChunk x tile | stages x kMaxP order | stages meta | barriers
+__host__ __device__ constexpr uint32_t chunked_smem_bytes(uint32_t tile) {
+  return (uint32_t)kCStages * kChunk * tile + (uint32_t)kCStages * kMaxP + (uint32_t)(kCStages * sizeof(ChunkMeta)) +
+         (uint32_t)(2 * kCStages * sizeof(uint64_t)) + 16u;
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(kBulkThreads, DDL_CHUNK_MINB) fold_chunked_kernel(const __grid_constant__ FoldParams p) {
+  constexpr int L = F16 ? 8 : 4;
+  constexpr int V = 2;  // columns per consumer thread: 2 x 256 x 16 B = 8 KB
+  extern __shared__ __align__(128) unsigned char smem[];
+  const uint32_t P = (uint32_t)p.P, T = p.tile_bytes;
+  unsigned char* stage = smem;
+  uint8_t* s_order = smem + (uint32_t)kCStages * kChunk * T;
+  ChunkMeta* s_meta = reinterpret_cast<ChunkMeta*>(s_order + kCStages * kMaxP);
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_meta + kCStages);
+  uint64_t* empty = full + kCStages;
+
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
+  const uint32_t my_n = p.n_items > blockIdx.x ? (p.n_items - 1u - blockIdx.x) / gridDim.x + 1u : 0u;
+  const uint32_t nq = (P + kChunk - 1) / kChunk;  // chunks per item
+  const uint32_t n_stages = my_n * nq;
+  const bool rh = F16 && p.round_hops;
+
+  if (tid == 0) {
+    for (int k = 0; k < kCStages; ++k) {
+      mbar_init(&full[k], 1);
+      mbar_init(&empty[k], kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  uint32_t issued = 0, consumed = 0;  // stages this thread's role got through
+  bool timed_out = false;
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer warp ----------------
+    for (uint32_t u = 0; u < n_stages; ++u) {
+      const uint32_t k = u % kCStages, s = u / nq, q = u % nq;
+      if (u >= (uint32_t)kCStages && !mbar_wait(&empty[k], ((u / kCStages) - 1u) & 1u)) {
+        timed_out = true;
+        break;
+      }
+      if (lane == 0) {
+        const Item item = p.items[p.item0 + blockIdx.x + s * gridDim.x];
+        ChunkMeta m;
+        m.eb = item.begin;
+        m.ee = item.begin + item.len;
+        m.vb = (m.eb + L - 1) / L;
+        m.ve = m.ee / L;
+        if (m.ve < m.vb) m.ve = m.vb;
+        m.t0 = q * kChunk;
+        m.nr = P - m.t0 < (uint32_t)kChunk ? P - m.t0 : (uint32_t)kChunk;
+        m.last = q + 1 == nq;
+        m.ok = item.seg < p.n_segs && (uint64_t)item.seg * P + P <= p.n_orders &&
+               (m.ve - m.vb) * 16u <= (uint64_t)T;
+        if (!m.ok) atomicOr(p.err, kErrBadItem);
+        s_meta[k] = m;
+      }
+      __syncwarp();
+      const ChunkMeta m = s_meta[k];
+      const uint32_t seg = p.items[p.item0 + blockIdx.x + s * gridDim.x].seg;
+      if (m.ok)
+        for (uint32_t t = lane; t < P; t += 32) {
+          const uint32_t r = p.orders[(uint64_t)seg * P + t];
+          s_order[k * kMaxP + t] = (uint8_t)(r < P ? r : 0);
+        }
+      const uint32_t bytes = m.ok ? (uint32_t)(m.ve - m.vb) * 16u : 0u;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&full[k], bytes * m.nr);  // release: meta and order are published
+      __syncwarp();
+      if (bytes && lane < m.nr) {
+        const uint32_t r = s_order[k * kMaxP + m.t0 + lane];
+        bulk_load(stage + ((size_t)k * kChunk + lane) * T, static_cast<const char*>(p.bufs[r]) + m.vb * 16u, bytes,
+                  &full[k]);
+      }
+      issued = u + 1;
+    }
+    if (timed_out && lane == 0) atomicOr(p.err, kErrWaitTimeout);
+  } else {
+    // ---------------- consumer warps ----------------
+    float in[V][L], out[V][L];
+    uint32_t hin[V][4] = {}, hout[V][4] = {};  // packed binary16 accumulators (rounded hops)
+    int h = 0, g = 0;
+    for (uint32_t u = 0; u < n_stages; ++u) {
+      const uint32_t k = u % kCStages;
+      if (!mbar_wait(&full[k], (u / kCStages) & 1u)) {
+        timed_out = true;
+        break;
+      }
+      const ChunkMeta m = s_meta[k];
+      const uint32_t ncols = (uint32_t)(m.ve - m.vb);
+      const int inner = p.inner, groups = p.groups;
+      if (m.t0 == 0) h = g = 0;
+      if (m.ok) {
+        const unsigned char* st = stage + (size_t)k * kChunk * T;
+        for (uint32_t j = 0; j < m.nr; ++j) {
+          const int t = (int)(m.t0 + j);
+          const Ctl c = ctl_at(t, h, g, inner, groups, (int)P, rh);
+#pragma unroll
+          for (int v = 0; v < V; ++v) {
+            const uint32_t col = tid + (uint32_t)v * kConsumers;
+            if (col >= ncols) continue;
+            const uint4 raw = *reinterpret_cast<const uint4*>(st + (size_t)j * T + col * 16u);
+            if constexpr (F16) {
+              if (rh && t < (int)P - 1) {
+                fold_h2(hin[v], hout[v], raw, c);
+                continue;
+              }
+              if (rh) {  // the last position: its final add stays binary32
+                widen_h2(hin[v], in[v]);
+                widen_h2(hout[v], out[v]);
+              }
+            }
+            float f[L];
+            unpack<F16>(raw, f);
+            fold_lanes<L>(in[v], out[v], f, c);
+          }
+          if (++h == inner) {
+            h = 0;
+            ++g;
+          }
+        }
+      }
+      if (m.ok && m.last) {  // before releasing the stage: the edge path reads its order
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          const uint32_t col = tid + (uint32_t)v * kConsumers;
+          if (col >= ncols) continue;
+          float r[L];
+#pragma unroll
+          for (int l = 0; l < L; ++l) r[l] = __fmul_rn(out[v][l], p.scale);
+          const uint4 res = pack<F16>(r);
+          for (uint32_t t = 0; t < P; ++t) __stcs(reinterpret_cast<uint4*>(p.bufs[t]) + m.vb + col, res);
+        }
+        // elements of a column cut by the item's ends: straight from global
+        const uint64_t nh = (m.ve > m.vb) ? m.vb * L - m.eb : m.ee - m.eb;
+        const uint64_t nt = (m.ve > m.vb) ? m.ee - m.ve * L : 0;
+        if (tid < nh + nt) {
+          const uint64_t e = tid < nh ? m.eb + tid : m.ve * L + (tid - nh);
+          fold_scalar_ordered<F16>(p, s_order + k * kMaxP, e, inner, groups, rh);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[k]);  // this warp is done with stage k
+      consumed = u + 1;
+    }
+    if (timed_out && lane == 0) atomicOr(p.err, kErrWaitTimeout);
+  }
+
+  // Both roles leave their loops (every wait is bounded).  Publish how far the
+  // producer got, then let loads that nobody consumed land before exit.
+  __shared__ uint32_t s_issued, s_consumed;
+  if (warp == kConsumerWarps && lane == 0) s_issued = issued;
+  if (tid == 0) s_consumed = consumed;
+  __syncthreads();
+  if (tid == 0)
+    for (uint32_t q = s_consumed; q < s_issued; ++q) mbar_wait(&full[q % kCStages], (q / kCStages) & 1u);
+}
+
+// ---------------------------------------------------------------------------
 // Variant 4: staged through shared memory by 2D tensor-map copies.  When the
 // P rank buffers are equally spaced (one slab, rank r at base + r * stride), a
 // tensor map of [P rows x N elements] lets one cp.async.bulk.tensor.2d fetch
@@ -1117,6 +1310,26 @@ cudaError_t launch_bulk(const FoldParams& p, uint32_t n_items, cudaStream_t stre
   return cudaGetLastError();
 }
 
+template <bool F16>
+cudaError_t launch_chunked(const FoldParams& p, uint32_t n_items, cudaStream_t stream) {
+  const uint32_t smem = chunked_smem_bytes(p.tile_bytes);
+  int dev = 0, sms = 0, max_smem = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  // two 16-byte columns per consumer thread cover a tile of at most 8 KB
+  if (smem > (uint32_t)max_smem || p.tile_bytes % 16 != 0 || p.tile_bytes == 0 ||
+      p.tile_bytes > 2u * (uint32_t)kConsumers * 16u)
+    return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(fold_chunked_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const uint32_t cap = (uint32_t)sms * DDL_CHUNK_MINB;
+  const uint32_t grid = n_items < cap ? n_items : cap;
+  fold_chunked_kernel<F16><<<grid, kBulkThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 // One CTA of kThreads per work item, optionally as a programmatic dependent.
 cudaError_t launch_items(void (*kernel)(FoldParams), const FoldParams& p, uint32_t n_items, cudaStream_t stream,
                          bool early) {
@@ -1176,6 +1389,8 @@ cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int var
     return f16 ? launch_bulk<true, true>(p, n_items, stream) : launch_bulk<false, true>(p, n_items, stream);
   if (variant == kVarBulkLoad)
     return f16 ? launch_bulk<true, false>(p, n_items, stream) : launch_bulk<false, false>(p, n_items, stream);
+  if (variant == kVarChunked)
+    return f16 ? launch_chunked<true>(p, n_items, stream) : launch_chunked<false>(p, n_items, stream);
   return f16 ? launch_ldg<true>(p, n_items, stream, early_launch) : launch_ldg<false>(p, n_items, stream, early_launch);
 }
 

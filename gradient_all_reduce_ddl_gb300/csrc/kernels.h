@@ -79,7 +79,7 @@ struct StepParams {
 };
 
 // Variants of the fused pass.
-enum FoldVariant : int { kVarLdg = 1, kVarBulk = 2, kVarBulkLoad = 3 };
+enum FoldVariant : int { kVarLdg = 1, kVarBulk = 2, kVarBulkLoad = 3, kVarChunked = 4 };
 
 // The staged pass whose loads are 2D tensor-map copies of [P ranks x box]
 // from equally spaced rank buffers (ddl_allreduce_slab).

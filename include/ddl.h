@@ -93,9 +93,13 @@ typedef enum {
   DDL_KERNEL_BULK = 2,  /* fused pass staged through shared memory by bulk async copies,
                            loads and stores */
   DDL_KERNEL_BULK_LOAD = 3, /* bulk async loads into shared memory, stores from registers */
-  DDL_KERNEL_TMA = 4        /* ddl_allreduce_slab only: 2D tensor-map loads of every rank's
+  DDL_KERNEL_TMA = 4,       /* ddl_allreduce_slab only: 2D tensor-map loads of every rank's
                                next tile in one copy, stores from registers (elsewhere and
                                when the slab does not qualify: the register pass) */
+  DDL_KERNEL_CHUNKED = 5    /* bulk async loads of the register pass's tiles (up to 8 KB per
+                               rank) into shared memory, 2 ranks per stage in fold order,
+                               the fold kept in registers across an item's stages, stores
+                               from registers */
 } ddl_kernel_t;
 
 typedef struct ddl_plan* ddl_plan_t;

@@ -190,3 +190,13 @@ def test_invalid_arguments(ddl):
         assert p.buckets() == [(0, 100)]
         ddl.ddl_plan_set_layers(p.handle, [50, 50])
         assert p.launches == 0
+
+
+def test_kernel_choice_range(ddl):
+    """Every ddl_kernel_t value is accepted on a host-only plan; the next one
+    is refused."""
+    with ddl.Plan(8, 10_000) as plan:
+        for k in range(0, 6):
+            assert ddl._lib.ddl_plan_set_kernel(plan.handle, k) == ddl.DDL_OK, k
+        assert ddl._lib.ddl_plan_set_kernel(plan.handle, 6) == ddl.DDL_ERR_INVALID_ARG
+        assert ddl._lib.ddl_plan_set_kernel(plan.handle, -1) == ddl.DDL_ERR_INVALID_ARG

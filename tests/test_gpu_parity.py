@@ -96,7 +96,7 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("kernel", ["ldg", "bulk", "bulkload"])
+@pytest.mark.parametrize("kernel", ["ldg", "bulk", "bulkload", "chunked"])
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
 def test_fused_matches_oracle(ddl, case, dtype, kernel):
@@ -105,7 +105,7 @@ def test_fused_matches_oracle(ddl, case, dtype, kernel):
     _check_exact(ddl, _w(dtype=dtype, **case), kernel=kernel)
 
 
-@pytest.mark.parametrize("kernel", ["ldg", "bulk"])
+@pytest.mark.parametrize("kernel", ["ldg", "bulk", "chunked"])
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
 @pytest.mark.parametrize("case", [SMALL[4], SMALL[7], SMALL[11], SMALL[16], SMALL[18]])
 def test_fused_unaligned_buffers_match_oracle(ddl, case, dtype, kernel):
@@ -376,7 +376,7 @@ FULL = ["ring4_int", "torus4x4_resnet50", "torus8x4_resnet50_f16", "multiring64_
         "multiring16_lm300m", "torus4x4_lm300m", "torus4x4x4_resnet101", "torus4x4x2_resnet50_f16"]
 
 
-@pytest.mark.parametrize("kernel", ["auto", "bulk", "bulkload"])
+@pytest.mark.parametrize("kernel", ["auto", "bulk", "bulkload", "chunked"])
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_workload_sampled(ddl, name, kernel):
     w = synth.WORKLOADS[name]
