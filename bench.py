@@ -48,6 +48,7 @@ NCU_TRAFFIC = {
     ("torus4x4_resnet50", "ldg", "2c4e6c02dcdb9dcd"): 1_635_898_368 + 1_576_063_744,
     ("torus4x4_resnet50", "ldg", "8b82de61611a4d5b"): 1_635_897_088 + 1_575_497_728,
     ("torus4x4_resnet50", "ldg", "11c73895f5e07e69"): 1_635_897_344 + 1_575_480_064,
+    ("torus4x4_resnet50", "ldg", "fcb0b1da26b97bdc"): 1_635_928_320 + 1_575_545_600,
 }
 
 KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]
