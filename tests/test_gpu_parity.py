@@ -336,6 +336,31 @@ def test_extreme_shapes_match_oracle(ddl, case, dtype):
     _check_exact(ddl, _w(dtype=dtype, **case))
 
 
+@pytest.mark.parametrize("kernel", ["auto", "chunked"])
+def test_largest_p_at_size_sampled(ddl, kernel):
+    """P = 256 ranks of 4,000,003 fp32 elements (4.1 GB resident), multi-ring
+    k = 8 in 3 MiB buckets: every rank pointer of the kernel's parameter
+    block in use at size.  Sampled against the oracle's closed form (random
+    and at every edge); all ranks identical."""
+    w = _w(P=256, N=4_000_003, topo="multiring", k=8, bucket_bytes=3 << 20, seed=256)
+    bufs = device_bufs_generated(w, DEV)
+    with ddl.Plan.for_workload(w, kernel=kernel) as plan:
+        plan.allreduce(bufs, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    for r in range(1, w.P):
+        assert torch.equal(bufs[r].view(torch.int32), bufs[0].view(torch.int32)), r
+    rng = np.random.default_rng(256)
+    idx = np.unique(np.concatenate([rng.integers(0, w.N, 20_000), edge_samples(w)]))
+    x_rows = np.stack([w.rank_values(r, idx.astype(np.uint64)) for r in range(w.P)], axis=1)
+    want = oracle.closed_form(oracle_cfg(w), x_rows, idx.astype(np.uint64), w.scale)
+    got = to_numpy_bits(bufs[0][torch.from_numpy(idx).to(DEV)])
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"{bad.size} of {idx.size} sampled elements differ, e.g. idx {idx[bad[:5]]}"
+    del bufs
+    torch.cuda.empty_cache()
+
+
 def test_more_than_2_32_elements_per_rank_sampled(ddl):
     """Element indices past 2^32: a 3-rank fp16 ring of 2^32 + 12,345 elements
     per rank (8.6 GB each) in 3 GiB buckets, so bucket and chunk edges and
