@@ -113,12 +113,14 @@ def test_workload_tables_match_oracle(ddl, name):
 
 
 @pytest.mark.parametrize("case", [CASES[2], CASES[5], CASES[7], CASES[9]])
-def test_staged_kernel_tables_match_oracle(ddl, case):
-    """Selecting the staged kernel rebuilds the work items at its tile size;
-    the fold orders stay the oracle's."""
+@pytest.mark.parametrize("kernel", ["bulk", "chunked"])
+def test_staged_kernel_tables_match_oracle(ddl, case, kernel):
+    """Selecting a staged kernel rebuilds the work items at its tile size (the
+    rank-chunked pass keeps the register pass's); the fold orders stay the
+    oracle's."""
     plan, cfg = _pair(**case)
     with plan:
-        plan.set_kernel("bulk")
+        plan.set_kernel(kernel)
         assert plan.buckets() == oracle.buckets(cfg)
         for i in range(cfg.N):
             o_ord, o_in, o_gr = oracle.fold_order(cfg, i)
