@@ -316,6 +316,59 @@ def test_device_generator_matches_host(ddl):
             assert np.array_equal(to_numpy_bits(dev[r]), w.rank_values(r)), (dist, dtype, r)
 
 
+@pytest.mark.parametrize("name", ["torus4x4_resnet50", "torus8x4_resnet50_f16", "multiring64_resnet101",
+                                  "torus4x4x4_resnet101"])
+def test_full_size_stepwise_sampled(ddl, name):
+    """The stepwise mode (one launch per communication step) at full size:
+    bit-exact with the oracle's closed form on sampled elements, ranks
+    identical."""
+    w = synth.WORKLOADS[name]
+    bufs = device_bufs_generated(w, DEV)
+    with ddl.Plan.for_workload(w, mode="stepwise") as plan:
+        plan.allreduce(bufs, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    view = torch.int16 if w.dtype == "f16" else torch.int32
+    for r in range(1, w.P):
+        assert torch.equal(bufs[r].view(view), bufs[0].view(view)), r
+    rng = np.random.default_rng(1234)
+    idx = np.unique(np.concatenate([rng.integers(0, w.N, 30_000), edge_samples(w)]))
+    x_rows = np.stack([w.rank_values(r, idx.astype(np.uint64)) for r in range(w.P)], axis=1)
+    want = oracle.closed_form(oracle_cfg(w), x_rows, idx.astype(np.uint64), w.scale)
+    got = to_numpy_bits(bufs[0][torch.from_numpy(idx).to(DEV)])
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"{bad.size} of {idx.size} sampled elements differ, e.g. idx {idx[bad[:5]]}"
+    del bufs
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,tol", [("torus4x4_resnet50", 1e-6), ("torus8x4_resnet50_f16", 2e-3),
+                                      ("ring16_lm300m", 1e-6)])
+def test_full_size_rankorder_within_tolerance(ddl, name, tol):
+    """The rank-order mode at full size: normwise error against the binary64
+    sum of the stored inputs (times the scale) on sampled elements, within
+    1e-6 (fp32) or 2e-3 (fp16); ranks identical."""
+    w = synth.WORKLOADS[name]
+    bufs = device_bufs_generated(w, DEV)
+    with ddl.Plan.for_workload(w, mode="rankorder") as plan:
+        plan.allreduce(bufs, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    view = torch.int16 if w.dtype == "f16" else torch.int32
+    for r in range(1, w.P):
+        assert torch.equal(bufs[r].view(view), bufs[0].view(view)), r
+    rng = np.random.default_rng(4321)
+    idx = np.unique(rng.integers(0, w.N, 200_000))
+    host = [w.rank_values(r, idx.astype(np.uint64)) for r in range(w.P)]
+    ref = oracle.ref64(host, w.scale, w.dtype)
+    got0 = to_numpy_bits(bufs[0][torch.from_numpy(idx).to(DEV)])
+    got = oracle.f16_to_f32(got0).astype(np.float64) if w.dtype == "f16" else got0.astype(np.float64)
+    err = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert err <= tol, err
+    del bufs
+    torch.cuda.empty_cache()
+
+
 # The largest P the plan takes (256: rank orders are stored as bytes) on every
 # schedule, and the smallest buffers (fewer elements than ranks or chunks).
 EXTREME = [
