@@ -599,6 +599,32 @@ def test_allreduce_host_zero_copy(ddl, case, dtype, kernel):
             assert e.status == ddl.DDL_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_allreduce_host_zero_copy_unaligned(ddl, dtype):
+    """Page-locked host buffers that start one element past a 16-byte
+    boundary: the zero-copy pass takes its element-wise path (the bulk copies
+    need 16-byte alignment) and still matches the oracle bit for bit."""
+    w = _w(P=8, N=60_001, dtype=dtype, topo="torus", X=4, Y=2, seed=61)
+    host = _host_inputs(w)
+    ref = [h.copy() for h in host]
+    oracle.emulate(oracle_cfg(w), ref, w.scale)
+    big = [torch.zeros(w.N + 1, dtype=torch.int16 if dtype == "f16" else torch.float32).pin_memory()
+           for _ in range(w.P)]
+    views = []
+    for b, h in zip(big, host):
+        v = b[1:]
+        v.copy_(torch.from_numpy(h.view(np.int16) if dtype == "f16" else h))
+        views.append(v)
+    with ddl.Plan.for_workload(w) as plan:
+        plan.allreduce_host(views, None, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    for r in range(w.P):
+        got = views[r].numpy()
+        got = got.view(np.uint16) if dtype == "f16" else got
+        assert np.array_equal(got, ref[r]), r
+
+
 def test_zero_copy_tables_follow_plan_changes(ddl):
     """The zero-copy pass's own work items are rebuilt when the plan changes:
     zero-copy, then a layer list (new buckets), zero-copy again, then
