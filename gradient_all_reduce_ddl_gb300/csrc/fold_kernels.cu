@@ -251,6 +251,8 @@ __global__ void __launch_bounds__(kThreads, MINB) fold_ldg_kernel(const __grid_c
   }
   float in[V][L], out[V][L];
   uint32_t hin[V][4] = {}, hout[V][4] = {};  // packed accumulators (H2)
+  uint4 xl[V];  // the last position's values (H2: folded after the loop)
+  Ctl cl = {};
   int h = 0, g = 0;
   for (int t0 = 0; t0 < P; t0 += B) {
     uint4 raw[B][V];
@@ -266,25 +268,38 @@ __global__ void __launch_bounds__(kThreads, MINB) fold_ldg_kernel(const __grid_c
     for (int j = 0; j < B; ++j) {
       if (t0 + j < P) {
         const Ctl c = ctl_at(t0 + j, h, g, inner, groups, P, rh);
+        if constexpr (H2) {
+          if (t0 + j < P - 1) {
 #pragma unroll
-        for (int u = 0; u < V; ++u) {
-          if constexpr (H2) {
-            if (t0 + j < P - 1) {
-              fold_h2(hin[u], hout[u], raw[j][u], c);
-              continue;
-            }
-            widen_h2(hin[u], in[u]);  // the last position: its final add stays binary32
-            widen_h2(hout[u], out[u]);
+            for (int u = 0; u < V; ++u) fold_h2(hin[u], hout[u], raw[j][u], c);
+          } else {
+#pragma unroll
+            for (int u = 0; u < V; ++u) xl[u] = raw[j][u];
+            cl = c;
           }
-          float f[L];
-          unpack<F16>(raw[j][u], f);
-          fold_lanes<L>(in[u], out[u], f, c);
+        } else {
+#pragma unroll
+          for (int u = 0; u < V; ++u) {
+            float f[L];
+            unpack<F16>(raw[j][u], f);
+            fold_lanes<L>(in[u], out[u], f, c);
+          }
         }
         if (++h == inner) {
           h = 0;
           ++g;
         }
       }
+    }
+  }
+  if constexpr (H2) {  // the last position: widen, its final add stays binary32
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      widen_h2(hin[u], in[u]);
+      widen_h2(hout[u], out[u]);
+      float f[L];
+      unpack<F16>(xl[u], f);
+      fold_lanes<L>(in[u], out[u], f, cl);
     }
   }
   uint4 res[V];
