@@ -49,6 +49,7 @@ NCU_TRAFFIC = {
     ("torus4x4_resnet50", "ldg", "8b82de61611a4d5b"): 1_635_897_088 + 1_575_497_728,
     ("torus4x4_resnet50", "ldg", "11c73895f5e07e69"): 1_635_897_344 + 1_575_480_064,
     ("torus4x4_resnet50", "ldg", "fcb0b1da26b97bdc"): 1_635_928_320 + 1_575_545_600,
+    ("torus4x4_resnet50", "ldg", "b611438140eeb7a2"): 1_635_899_136 + 1_575_681_792,
 }
 
 KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]
