@@ -522,6 +522,21 @@ def main():
     gbs = job_gbs(nbytes, ws, ms_per_step)
     elems = w.P * w.N * ws / (ms_per_step * 1e-3)
 
+    # spread: 20 more steps, each bracketed by its own events (outside the
+    # timed region; only where a step is long enough that two event records
+    # per step do not distort it)
+    step_median_ms = None
+    if graph is None and ms_per_step > 0.05:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(21)]
+        evs[0].record(stream)
+        for i in range(20):
+            plan.allreduce(bufs, w.scale, stream)
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        per = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(20))
+        step_median_ms = {"median": round(0.5 * (per[9] + per[10]), 5), "min": round(per[0], 5),
+                          "max": round(per[-1], 5), "steps": 20}
+
     # roofline of the dominant kernel: one fused launch per bucket
     nb = plan.num_buckets
     launches_per_call = max(1, launches // args.steps)
@@ -622,6 +637,7 @@ def main():
                            "launch": (f"CUDA graph replay, {per_graph} all-reduces per graph" if args.graph
                                       else "ddl_allreduce call per step"),
                            "elems_per_s": round(elems, 1), "frac_of_hbm": round(gbs / ws / peak, 4),
+                           "step_ms_spread": step_median_ms,
                            "l2": (f"inputs {w.P * w.N * w.esize / 1e9:.2f} GB per replica, larger than the 129 MB L2"
                                   if w.P * w.N * w.esize > 129e6 else
                                   f"inputs {w.P * w.N * w.esize / 1e6:.1f} MB fit in the 129 MB L2: back-to-back "
