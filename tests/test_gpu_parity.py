@@ -369,6 +369,46 @@ def test_full_size_rankorder_within_tolerance(ddl, name, tol):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("name", ["torus4x4_resnet50", "torus8x4_resnet50_f16", "multiring64_resnet101"])
+def test_full_size_sgd_sampled(ddl, name):
+    """The all-reduce fused with momentum SGD at full size, as the bench's
+    --sgd study runs it.  On sampled elements: the stored averaged gradient
+    from the oracle's closed form; the update of two ranks' own parameters and
+    momenta (different on each rank) from the oracle's SGD on a one-rank
+    problem fed that gradient (a one-rank all-reduce with scale 1 leaves it
+    unchanged, so only the update remains)."""
+    w = synth.WORKLOADS[name]
+    lr, mu, wd = 0.01, 0.9, 1e-4
+    bufs = device_bufs_generated(w, DEV)
+    params, moms = [], []
+    for r in range(w.P):
+        pt = torch.empty(w.N, dtype=torch.float32, device=DEV)
+        mt = torch.empty(w.N, dtype=torch.float32, device=DEV)
+        synth.fill_device(pt.data_ptr(), w.N, w.seed + 100, r, "normal", 1.0, "f32")
+        synth.fill_device(mt.data_ptr(), w.N, w.seed + 200, r, "normal", 0.1, "f32")
+        params.append(pt)
+        moms.append(mt)
+    with ddl.Plan.for_workload(w) as plan:
+        plan.allreduce_sgd(bufs, params, moms, w.scale, lr, mu, wd, keep_grads=True)
+        torch.cuda.synchronize()
+        plan.check()
+    rng = np.random.default_rng(99)
+    idx = np.unique(np.concatenate([rng.integers(0, w.N, 20_000), edge_samples(w)[::7]]))
+    x_rows = np.stack([w.rank_values(r, idx.astype(np.uint64)) for r in range(w.P)], axis=1)
+    g = oracle.closed_form(oracle_cfg(w), x_rows, idx.astype(np.uint64), w.scale)
+    t_idx = torch.from_numpy(idx).to(DEV)
+    assert np.array_equal(to_numpy_bits(bufs[0][t_idx]), g)
+    one = oracle.Config(1, idx.size, w.dtype, "ring")
+    for r in (0, w.P - 1):
+        p_want = synth.draw(w.seed + 100, r, idx.astype(np.uint64), "normal", 1.0, "f32").copy()
+        m_want = synth.draw(w.seed + 200, r, idx.astype(np.uint64), "normal", 0.1, "f32").copy()
+        oracle.sgd(one, [g.copy()], [p_want], [m_want], 1.0, lr, mu, wd)
+        assert np.array_equal(params[r][t_idx].cpu().numpy(), p_want), ("params", r)
+        assert np.array_equal(moms[r][t_idx].cpu().numpy(), m_want), ("moms", r)
+    del bufs, params, moms
+    torch.cuda.empty_cache()
+
+
 # The largest P the plan takes (256: rank orders are stored as bytes) on every
 # schedule, and the smallest buffers (fewer elements than ranks or chunks).
 EXTREME = [
