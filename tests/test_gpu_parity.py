@@ -557,6 +557,46 @@ def test_overlap_with_backward_matches_allreduce(ddl):
         assert np.array_equal(to_numpy_bits(bufs[r]), ref[r])
 
 
+@pytest.mark.parametrize("name", ["multiring64_resnet101", "torus4x4x4_resnet101"])
+def test_full_size_overlap_sampled(ddl, name):
+    """The bucket scheduler at full size: the 7 ResNet-101 buckets written
+    from a producer stream in reverse-layer order and each signalled as it
+    completes, reduced on the plan's side stream.  Sampled against the
+    oracle's closed form (random and at every edge); ranks identical."""
+    w = synth.WORKLOADS[name]
+    src = device_bufs_generated(w, DEV)
+    bufs = [torch.zeros(w.N, dtype=torch_dtype(w.dtype), device=DEV) for _ in range(w.P)]
+    torch.cuda.synchronize()
+    main = torch.cuda.Stream()
+    with ddl.Plan.for_workload(w) as plan:
+        nb = plan.num_buckets
+        assert nb == 7
+        with torch.cuda.stream(main):
+            plan.overlap_begin(bufs, w.scale, stream=main)
+            for b in range(nb):
+                lo, hi = plan.bucket_range(b)
+                for r in range(w.P):
+                    bufs[r][lo:hi].copy_(src[r][lo:hi])
+                plan.bucket_ready(b, stream=main)
+            plan.overlap_end(stream=main)
+        main.synchronize()
+        torch.cuda.synchronize()
+        plan.check()
+    del src
+    view = torch.int16 if w.dtype == "f16" else torch.int32
+    for r in range(1, w.P):
+        assert torch.equal(bufs[r].view(view), bufs[0].view(view)), r
+    rng = np.random.default_rng(7)
+    idx = np.unique(np.concatenate([rng.integers(0, w.N, 20_000), edge_samples(w)]))
+    x_rows = np.stack([w.rank_values(r, idx.astype(np.uint64)) for r in range(w.P)], axis=1)
+    want = oracle.closed_form(oracle_cfg(w), x_rows, idx.astype(np.uint64), w.scale)
+    got = to_numpy_bits(bufs[0][torch.from_numpy(idx).to(DEV)])
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"{bad.size} of {idx.size} sampled elements differ, e.g. idx {idx[bad[:5]]}"
+    del bufs
+    torch.cuda.empty_cache()
+
+
 def test_allreduce_host_buffers(ddl):
     w = _w(P=6, N=50_001, topo="torus", X=3, Y=2, seed=8)
     host = _host_inputs(w)
