@@ -597,6 +597,36 @@ def test_full_size_overlap_sampled(ddl, name):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("name", ["torus4x4_resnet50", "torus8x4_resnet50_f16"])
+def test_full_size_zero_copy_sampled(ddl, name):
+    """The end-to-end form as the bench times it: full-size gradients in
+    page-locked host memory, reduced in place over the host link (the
+    bulk-load pass over its own work items).  Sampled against the oracle's
+    closed form; every rank's host buffer identical."""
+    w = synth.WORKLOADS[name]
+    dev = device_bufs_generated(w, DEV)
+    host = [torch.empty(w.N, dtype=torch_dtype(w.dtype), pin_memory=True) for _ in range(w.P)]
+    for r in range(w.P):
+        host[r].copy_(dev[r])
+    del dev
+    torch.cuda.synchronize()
+    with ddl.Plan.for_workload(w) as plan:
+        plan.allreduce_host(host, None, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    view = torch.int16 if w.dtype == "f16" else torch.int32
+    for r in range(1, w.P):
+        assert torch.equal(host[r].view(view), host[0].view(view)), r
+    rng = np.random.default_rng(11)
+    idx = np.unique(np.concatenate([rng.integers(0, w.N, 20_000), edge_samples(w)]))
+    x_rows = np.stack([w.rank_values(r, idx.astype(np.uint64)) for r in range(w.P)], axis=1)
+    want = oracle.closed_form(oracle_cfg(w), x_rows, idx.astype(np.uint64), w.scale)
+    got = to_numpy_bits(host[0][torch.from_numpy(idx)])
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"{bad.size} of {idx.size} sampled elements differ, e.g. idx {idx[bad[:5]]}"
+    del host
+
+
 def test_allreduce_host_buffers(ddl):
     w = _w(P=6, N=50_001, topo="torus", X=3, Y=2, seed=8)
     host = _host_inputs(w)
