@@ -811,6 +811,35 @@ def test_back_to_back_calls_and_producer_kernels(ddl, case):
         assert np.array_equal(to_numpy_bits(bufs[r]), ref[r]), r
 
 
+def test_two_plans_on_two_streams_concurrently(ddl):
+    """Two plans (different schedules and dtypes) queued on two streams with no
+    ordering between them, each on its own buffers: both results match the
+    oracle (the plans share nothing on the device)."""
+    wa = _w(P=16, N=300_001, topo="torus", X=4, Y=4, seed=71)
+    wb = _w(P=12, N=250_003, dtype="f16", topo="multiring", k=2, bucket_bytes=200_000, seed=72)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    out = []
+    with ddl.Plan.for_workload(wa) as pa, ddl.Plan.for_workload(wb) as pb:
+        for w in (wa, wb):
+            host = _host_inputs(w)
+            ref = [h.copy() for h in host]
+            oracle.emulate(oracle_cfg(w), ref, w.scale)
+            out.append((w, device_bufs_from_host(host, DEV), ref))
+        torch.cuda.synchronize()
+        for _ in range(3):   # three rounds each, interleaved on the host, unordered on the GPU
+            pa.allreduce(out[0][1], wa.scale, stream=sa)
+            pb.allreduce(out[1][1], wb.scale, stream=sb)
+        torch.cuda.synchronize()
+        pa.check()
+        pb.check()
+    for w, bufs, ref in out:
+        ref3 = [r.copy() for r in ref]
+        oracle.emulate(oracle_cfg(w), ref3, w.scale)
+        oracle.emulate(oracle_cfg(w), ref3, w.scale)
+        for r in range(w.P):
+            assert np.array_equal(to_numpy_bits(bufs[r]), ref3[r]), (w.topo, r)
+
+
 def test_allreduce_captured_in_cuda_graph(ddl):
     """After a first (uploading) call, ddl_allreduce can be captured in a CUDA
     graph; each replay reduces whatever the buffers hold at that time."""
