@@ -637,6 +637,7 @@ def main():
                            "launch": (f"CUDA graph replay, {per_graph} all-reduces per graph" if args.graph
                                       else "ddl_allreduce call per step"),
                            "elems_per_s": round(elems, 1), "frac_of_hbm": round(gbs / ws / peak, 4),
+                           "frac_of_nominal_hbm": round(gbs / ws / 7900.0, 4),
                            "step_ms_spread": step_median_ms,
                            "l2": (f"inputs {w.P * w.N * w.esize / 1e9:.2f} GB per replica, larger than the 129 MB L2"
                                   if w.P * w.N * w.esize > 129e6 else
