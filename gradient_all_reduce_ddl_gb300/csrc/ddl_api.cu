@@ -822,11 +822,14 @@ ddl_status_t ddl_plan_traffic(ddl_plan_t p, uint64_t* moved, uint64_t* steps) {
   return DDL_OK;
 }
 
-ddl_status_t ddl_plan_cost(ddl_plan_t p, double alpha_s, double beta_s_per_byte, double* seconds) {
-  if (!p || !seconds || !(alpha_s >= 0.0) || !(beta_s_per_byte >= 0.0)) return DDL_ERR_INVALID_ARG;
-  *seconds = (double)p->tab.nsteps * alpha_s +
-             (double)p->tab.step_max_sum * (double)p->spec.esize * beta_s_per_byte;
-  return DDL_OK;
+ddl_status_t ddl_plan_cost(ddl_plan_t p, double alpha_s, double beta_s_per_byte, int links_per_worker,
+                           double* seconds) {
+  if (!p || !seconds || !(alpha_s >= 0.0) || !(beta_s_per_byte >= 0.0) || links_per_worker < 1)
+    return DDL_ERR_INVALID_ARG;
+  // the step tables of the schedule, whatever the plan's own mode
+  ddl::Spec s = p->spec;
+  s.mode = ddl::kStepwise;
+  return ddl::schedule_cost(s, alpha_s, beta_s_per_byte, links_per_worker, seconds) ? DDL_OK : DDL_ERR_OOM;
 }
 
 ddl_status_t ddl_plan_fold_order(ddl_plan_t p, size_t i, int32_t* order, int32_t* inner, int32_t* groups) {

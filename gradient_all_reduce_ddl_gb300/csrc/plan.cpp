@@ -82,6 +82,11 @@ struct Builder {
   Tables* t;
   bool with_steps;
   std::vector<int> mult;
+  // cost model: links per worker; the elements each (worker, link) pair
+  // sends in the step being built; their maximum summed over the steps
+  int links = 1;
+  std::vector<uint64_t> load;
+  uint64_t busiest_sum = 0;
 
   void add_segment(uint64_t lo, uint64_t len, const std::vector<int>& order, int inner, int groups) {
     if (len == 0) return;
@@ -163,11 +168,16 @@ struct Builder {
 
   // ---- message lists of the step-by-step schedule ----
   std::vector<Xfer> cur;
-  uint64_t step_max = 0;  // largest message of the step being built
 
-  void msg(uint64_t lo, uint64_t len, int src, int dst, uint32_t op) {
+  // ring: which of the step's concurrent rings carries the message (the
+  // multi-ring slice); it travels on link ring mod links of its sender
+  void msg(uint64_t lo, uint64_t len, int src, int dst, uint32_t op, int ring = 0) {
     t->moved += (op == kScaleOnly) ? 0 : len;
-    if (op != kScaleOnly && len > step_max) step_max = len;
+    if (op != kScaleOnly) {
+      const size_t at = (size_t)src * (size_t)links + (size_t)(ring % links);
+      if (load.size() < (size_t)s.P * (size_t)links) load.assign((size_t)s.P * (size_t)links, 0);
+      load[at] += len;
+    }
     if (!with_steps) return;
     Xfer x{};
     x.lo = lo;
@@ -178,27 +188,30 @@ struct Builder {
     cur.push_back(x);
   }
   // ring positions `ring`, elements [lo, lo+n), reduce-scatter step s
-  void rs(const std::vector<int>& ring, uint64_t lo, uint64_t n, int step, bool owner_final) {
+  void rs(const std::vector<int>& ring, uint64_t lo, uint64_t n, int step, bool owner_final, int ring_id = 0) {
     const int m = (int)ring.size();
     for (int p = 0; p < m; ++p) {
       const int c = ((p - step) % m + m) % m;
       const bool fin = owner_final && step == m - 2;
-      msg(lo + part_lo(n, m, c), part_len(n, m, c), ring[p], ring[(p + 1) % m], fin ? kAddFinal : kAddHop);
+      msg(lo + part_lo(n, m, c), part_len(n, m, c), ring[p], ring[(p + 1) % m], fin ? kAddFinal : kAddHop,
+          ring_id);
     }
   }
-  void ag(const std::vector<int>& ring, uint64_t lo, uint64_t n, int step) {
+  void ag(const std::vector<int>& ring, uint64_t lo, uint64_t n, int step, int ring_id = 0) {
     const int m = (int)ring.size();
     for (int p = 0; p < m; ++p) {
       const int c = ((p + 1 - step) % m + m) % m;
-      msg(lo + part_lo(n, m, c), part_len(n, m, c), ring[p], ring[(p + 1) % m], kCopy);
+      msg(lo + part_lo(n, m, c), part_len(n, m, c), ring[p], ring[(p + 1) % m], kCopy, ring_id);
     }
   }
   void close_step(bool communication) {
     if (communication) {
       ++t->nsteps;
-      t->step_max_sum += step_max;
+      uint64_t busiest = 0;
+      for (uint64_t v : load) busiest = std::max(busiest, v);
+      busiest_sum += busiest;
     }
-    step_max = 0;
+    std::fill(load.begin(), load.end(), 0);
     if (!with_steps) return;
     Step st{};
     st.xfer_begin = (uint32_t)t->xfers.size();
@@ -228,11 +241,11 @@ struct Builder {
       for (int j = 0; j < k; ++j)
         for (int p = 0; p < P; ++p) rings[j][p] = (int)((int64_t)p * (s.topo == kRing ? 1 : mult[j]) % P);
       for (int st = 0; st < P - 1; ++st) {
-        for (int j = 0; j < k; ++j) rs(rings[j], b.lo + part_lo(n, k, j), part_len(n, k, j), st, true);
+        for (int j = 0; j < k; ++j) rs(rings[j], b.lo + part_lo(n, k, j), part_len(n, k, j), st, true, j);
         close_step(true);
       }
       for (int st = 0; st < P - 1; ++st) {
-        for (int j = 0; j < k; ++j) ag(rings[j], b.lo + part_lo(n, k, j), part_len(n, k, j), st);
+        for (int j = 0; j < k; ++j) ag(rings[j], b.lo + part_lo(n, k, j), part_len(n, k, j), st, j);
         close_step(true);
       }
       return;
@@ -414,6 +427,22 @@ bool build_tables(const Spec& s, bool with_steps, Tables* t) {
     return true;
   } catch (const std::bad_alloc&) {
     *t = Tables();
+    return false;
+  }
+}
+
+bool schedule_cost(const Spec& s, double alpha, double beta, int links, double* seconds) {
+  try {
+    Tables t;
+    make_buckets(s, &t.buckets);
+    Builder bld{s, &t, false, {}};
+    // more links than concurrent rings carry nothing
+    bld.links = std::max(1, std::min(links, s.topo == kMultiRing ? s.k : 1));
+    if (s.topo == kMultiRing) ring_multipliers(s.P, s.k, &bld.mult);
+    for (const Bucket& b : t.buckets) bld.step_bucket(b);
+    *seconds = (double)t.nsteps * alpha + (double)bld.busiest_sum * (double)s.esize * beta;
+    return true;
+  } catch (const std::bad_alloc&) {
     return false;
   }
 }

@@ -95,7 +95,6 @@ struct Tables {
   std::vector<Step> steps;
   uint64_t moved = 0;   // elements sent over all messages
   uint64_t nsteps = 0;  // sequential communication steps
-  uint64_t step_max_sum = 0;  // sum over steps of the step's largest message (elements)
 };
 
 // Returns "" if the spec is valid, else a reason.  unsupported is set when the
@@ -109,6 +108,12 @@ bool ring_multipliers(int P, int k, std::vector<int>* out);
 // step/message tables (steps only listed when with_steps).  Returns false on
 // allocation failure.
 bool build_tables(const Spec& s, bool with_steps, Tables* t);
+
+// alpha-beta time of the schedule on P workers with `links` network links
+// each: every step costs alpha plus beta times the bytes of the busiest
+// (worker, link) pair, the message of concurrent ring j going on link
+// j mod links.  False on allocation failure.
+bool schedule_cost(const Spec& s, double alpha, double beta, int links, double* seconds);
 
 // Fold order of element i from the built tables.
 bool fold_order_of(const Spec& s, const Tables& t, uint64_t i, int32_t* order, int32_t* inner, int32_t* groups);

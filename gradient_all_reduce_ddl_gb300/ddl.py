@@ -74,7 +74,7 @@ _sig("ddl_overlap_end", _i, _vp, _vp)
 _sig("ddl_plan_num_buckets", _i, _vp, _P(_i))
 _sig("ddl_plan_bucket_range", _i, _vp, _i, _P(_sz), _P(_sz))
 _sig("ddl_plan_traffic", _i, _vp, _P(_u64), _P(_u64))
-_sig("ddl_plan_cost", _i, _vp, ctypes.c_double, ctypes.c_double, _P(ctypes.c_double))
+_sig("ddl_plan_cost", _i, _vp, ctypes.c_double, ctypes.c_double, _i, _P(ctypes.c_double))
 _sig("ddl_plan_fold_order", _i, _vp, _sz, _P(ctypes.c_int32), _P(ctypes.c_int32), _P(ctypes.c_int32))
 _sig("ddl_plan_launches", _i, _vp, _P(_u64))
 _sig("ddl_plan_check", _i, _vp)
@@ -209,9 +209,9 @@ def ddl_plan_traffic(plan):
     return m.value, s.value
 
 
-def ddl_plan_cost(plan, alpha_s, beta_s_per_byte):
+def ddl_plan_cost(plan, alpha_s, beta_s_per_byte, links_per_worker=1):
     t = ctypes.c_double()
-    _ok(_lib.ddl_plan_cost(plan, alpha_s, beta_s_per_byte, ctypes.byref(t)), "ddl_plan_cost")
+    _ok(_lib.ddl_plan_cost(plan, alpha_s, beta_s_per_byte, links_per_worker, ctypes.byref(t)), "ddl_plan_cost")
     return t.value
 
 
@@ -343,9 +343,10 @@ class Plan:
     def fold_order(self, i):
         return ddl_plan_fold_order(self.handle, i, self.P)
 
-    def cost(self, alpha_s, beta_s_per_byte):
-        """alpha-beta model of this schedule on P real workers (seconds)."""
-        return ddl_plan_cost(self.handle, alpha_s, beta_s_per_byte)
+    def cost(self, alpha_s, beta_s_per_byte, links=1):
+        """alpha-beta model of this schedule on P real workers with `links`
+        network links each (seconds)."""
+        return ddl_plan_cost(self.handle, alpha_s, beta_s_per_byte, links)
 
     @property
     def launches(self):

@@ -274,17 +274,26 @@ ddl_status_t ddl_plan_bucket_range(ddl_plan_t plan, int bucket, size_t* begin, s
  * 2(X-1)+2(Y-1), per bucket).  Host-only. */
 ddl_status_t ddl_plan_traffic(ddl_plan_t plan, uint64_t* elems_moved_total, uint64_t* steps);
 
-/* alpha-beta cost of the schedule on a cluster of P real workers: every
- * communication step costs alpha_s (latency) plus beta_s_per_byte times the
- * bytes of the step's largest message (each worker sends one message per step
- * on its own link, all at once); the all-reduce costs the sum over its steps
- * and buckets.  Ring: 2(P-1)(alpha + (n/P)e beta); torus: 2(X-1)(alpha +
- * (n/X)e beta) + 2(Y-1)(alpha + (n/(XY))e beta).  This is the latency /
- * bandwidth trade-off that "[论文解读] PowerAI DDL" (abstract) names for its
- * multi-ring pattern; the Baidu write-up's example (1.2 GB gradient, about
- * 6 GB/s InfiniBand, about 400 ms per iteration) is this model with
- * alpha = 0.  Host-only.  alpha_s, beta_s_per_byte >= 0. */
-ddl_status_t ddl_plan_cost(ddl_plan_t plan, double alpha_s, double beta_s_per_byte, double* seconds);
+/* alpha-beta cost of the schedule on a cluster of P real workers, each with
+ * links_per_worker (>= 1) network links.  In every communication step all
+ * workers send at once; a worker's message of concurrent ring j travels on
+ * its link j mod links_per_worker, messages sharing a link one after another;
+ * the step costs alpha_s (latency) plus beta_s_per_byte times the bytes of
+ * the busiest link of any worker; the all-reduce costs the sum over its steps
+ * and buckets.  Ring and torus send one message per worker per step:
+ * 2(P-1)(alpha + (n/P)e beta) and 2(X-1)(alpha + (n/X)e beta) +
+ * 2(Y-1)(alpha + (n/(XY))e beta), for any link count.  A k-ring multi-ring
+ * sends k messages of about n/(kP) elements per worker per step: with one
+ * link it costs what the ring costs (plus the ragged splits), with k links
+ * its bandwidth term shrinks k-fold.  This is the latency / bandwidth
+ * trade-off that "[论文解读] PowerAI DDL" (ABSTRACT) names for its multi-ring
+ * pattern; one link per worker compares the three schedules on equal
+ * hardware.  The Baidu write-up's example (a 1.2 GB gradient, about 6 GB/s
+ * InfiniBand, about 400 ms per iteration; final page, opening paragraphs) is
+ * the ring in this model with alpha = 0.  Host-only.  alpha_s,
+ * beta_s_per_byte >= 0; DDL_ERR_INVALID_ARG otherwise. */
+ddl_status_t ddl_plan_cost(ddl_plan_t plan, double alpha_s, double beta_s_per_byte, int links_per_worker,
+                           double* seconds);
 
 /* Introspection: the fold order of element i as the plan's tables hold it:
  * order[0..P-1] = ranks in the order they are added, *inner = group length

@@ -14,7 +14,8 @@ Parity status per function:
   buckets       pinned (hand-computed layer packing, closed form of fixed buckets)
   f32_to_f16    pinned (exhaustive against numpy's and the C compiler's binary16)
   ref64         pinned (integer inputs: exact sums)
-  cost          pinned (closed forms; the 400 ms language-model example)
+  cost          pinned (closed forms; the 400 ms language-model example; a hand-worked
+                P=4, k=2 multi-ring on one shared link and on a link per ring)
   sgd           pinned (exact dyadic arithmetic; torch.optim.SGD within one rounding)
 
 Buffers are numpy arrays: float32 for fp32, uint16 bit patterns for fp16.
@@ -86,7 +87,8 @@ def _load():
             lib.oracle_ring_strides.restype = ctypes.c_int
             lib.oracle_ref64.argtypes = [i32, u64, i32, P, ctypes.c_double, P]
             lib.oracle_ref64.restype = None
-            lib.oracle_cost.argtypes = [cfgp, ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
+            lib.oracle_cost.argtypes = [cfgp, ctypes.c_double, ctypes.c_double, ctypes.c_int32,
+                                        ctypes.POINTER(ctypes.c_double)]
             lib.oracle_cost.restype = ctypes.c_int
             lib.oracle_sgd.argtypes = [cfgp, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                        ctypes.c_float]
@@ -166,12 +168,13 @@ def traffic(cfg: Config):
     return emulate(cfg, None, 1.0)
 
 
-def cost(cfg: Config, alpha: float, beta: float) -> float:
-    """alpha-beta seconds of the schedule on P real workers (per-step largest
-    message, steps in sequence)."""
+def cost(cfg: Config, alpha: float, beta: float, links: int = 1) -> float:
+    """alpha-beta seconds of the schedule on P real workers with `links`
+    network links each: per step alpha plus beta times the bytes of the
+    busiest link (ring j of a step on link j mod links), steps in sequence."""
     lib = _load()
     t = ctypes.c_double()
-    _check(lib.oracle_cost(cfg._ref(), alpha, beta, ctypes.byref(t)))
+    _check(lib.oracle_cost(cfg._ref(), alpha, beta, int(links), ctypes.byref(t)))
     return t.value
 
 

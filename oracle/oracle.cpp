@@ -49,6 +49,12 @@
  *     to binary16 (RNE, subnormals kept, overflow to inf); the owner's last
  *     add stays binary32, is multiplied by the scale, then rounded once.
  *  R7 the scale is a binary32 multiplier applied once per element.
+ *  R8 cost model: a worker has `links` network links; in a step every worker
+ *     sends its messages at once, ring j's on link j mod links, so messages
+ *     sharing a link queue behind each other; the step lasts alpha plus beta
+ *     times the bytes of the busiest link.  One link per worker puts every
+ *     schedule on the same hardware; links = k lets the k rings of a
+ *     multi-ring run side by side.
  */
 #include <algorithm>
 #include <cstdint>
@@ -230,6 +236,7 @@ struct Bufs {
 /* One point-to-point message of one step. */
 struct Msg {
   int src, dst;
+  int ring;    /* which of the concurrent rings of the step carries it */
   uint64_t lo, hi;
   bool add;    /* reduce-scatter: receiver adds; all-gather: receiver copies */
   bool fin;    /* this add is the owner's last: scale, then store */
@@ -241,15 +248,18 @@ struct Emu {
   const Bufs* b; /* null: count traffic only */
   float scale;
   int64_t stop_after; /* number of steps to run; < 0 = all */
+  int links = 1;       /* network links per worker (cost model, R8) */
   uint64_t moved = 0, steps = 0;
-  uint64_t step_max_sum = 0; /* sum over steps of the largest message (elements) */
+  uint64_t step_load_sum = 0; /* sum over steps of the busiest link's elements (R8) */
   bool stopped = false;
   std::vector<Msg> pending;
 
   Emu(const Cfg& cfg, const Bufs* bufs, float s, int64_t stop) : c(cfg), b(bufs), scale(s), stop_after(stop) {}
 
-  /* ring over positions ring[0..m-1] on elements [lo, hi) */
-  void rs_send(const std::vector<int>& ring, uint64_t lo, uint64_t hi, int s, bool last_is_final) {
+  /* ring over positions ring[0..m-1] on elements [lo, hi); ring_id tells the
+   * step's concurrent rings apart (multi-ring slice j) */
+  void rs_send(const std::vector<int>& ring, uint64_t lo, uint64_t hi, int s, bool last_is_final,
+               int ring_id = 0) {
     const int m = (int)ring.size();
     const uint64_t n = hi - lo;
     for (int t = 0; t < m; ++t) {
@@ -257,6 +267,7 @@ struct Emu {
       Msg g;
       g.src = ring[t];
       g.dst = ring[(t + 1) % m];
+      g.ring = ring_id;
       g.lo = lo + part_start(n, m, ch);
       g.hi = g.lo + part_size(n, m, ch);
       g.add = true;
@@ -264,7 +275,7 @@ struct Emu {
       pending.push_back(std::move(g));
     }
   }
-  void ag_send(const std::vector<int>& ring, uint64_t lo, uint64_t hi, int s) {
+  void ag_send(const std::vector<int>& ring, uint64_t lo, uint64_t hi, int s, int ring_id = 0) {
     const int m = (int)ring.size();
     const uint64_t n = hi - lo;
     for (int t = 0; t < m; ++t) {
@@ -272,6 +283,7 @@ struct Emu {
       Msg g;
       g.src = ring[t];
       g.dst = ring[(t + 1) % m];
+      g.ring = ring_id;
       g.lo = lo + part_start(n, m, ch);
       g.hi = g.lo + part_size(n, m, ch);
       g.add = false;
@@ -293,10 +305,20 @@ struct Emu {
       pending.clear();
       return;
     }
-    uint64_t biggest = 0;
+    /* R8: the elements each (worker, link) pair sends in this step; ring j
+     * uses link j mod links */
+    std::vector<std::pair<std::pair<int, int>, uint64_t>> load;
+    for (const Msg& g : pending) {
+      const std::pair<int, int> key(g.src, g.ring % links);
+      bool found = false;
+      for (auto& e : load)
+        if (e.first == key) { e.second += g.hi - g.lo; found = true; break; }
+      if (!found) load.push_back({key, g.hi - g.lo});
+    }
+    uint64_t busiest = 0;
+    for (const auto& e : load) busiest = std::max(busiest, e.second);
     for (Msg& g : pending) {
       moved += g.hi - g.lo;
-      if (g.hi - g.lo > biggest) biggest = g.hi - g.lo;
       if (!b) continue;
       g.data.resize(g.hi - g.lo);
       for (uint64_t i = g.lo; i < g.hi; ++i) g.data[i - g.lo] = b->raw(g.src, i);
@@ -314,7 +336,7 @@ struct Emu {
     }
     pending.clear();
     ++steps;
-    step_max_sum += biggest;
+    step_load_sum += busiest;
   }
 
   void ring_bucket(uint64_t lo, uint64_t hi) {
@@ -335,7 +357,7 @@ struct Emu {
     for (int s = 0; s + 1 < c.P; ++s) {
       for (int j = 0; j < c.k; ++j) {
         const uint64_t a = lo + part_start(n, c.k, j);
-        rs_send(rings[j], a, a + part_size(n, c.k, j), s, true);
+        rs_send(rings[j], a, a + part_size(n, c.k, j), s, true, j);
       }
       step();
     }
@@ -343,7 +365,7 @@ struct Emu {
     for (int s = 0; s + 1 < c.P; ++s) {
       for (int j = 0; j < c.k; ++j) {
         const uint64_t a = lo + part_start(n, c.k, j);
-        ag_send(rings[j], a, a + part_size(n, c.k, j), s);
+        ag_send(rings[j], a, a + part_size(n, c.k, j), s, j);
       }
       step();
     }
@@ -639,16 +661,20 @@ int oracle_emulate(const oracle_cfg* cfg, void* const* bufs, float scale, int64_
   return 0;
 }
 
-/* alpha-beta time of the schedule on P real workers: each step costs
- * alpha + beta * (bytes of its largest message), all ranks sending at once;
- * steps add up.  From the emulation's own message lists. */
-int oracle_cost(const oracle_cfg* cfg, double alpha, double beta, double* seconds) {
+/* R8, alpha-beta time of the schedule on P real workers, each with `links`
+ * network links: in every step all workers send at once; a worker's messages
+ * of concurrent ring j travel on its link j mod links, one after another; the
+ * step costs alpha + beta * (bytes on the busiest link of any worker); steps
+ * add up.  From the emulation's own message lists. */
+int oracle_cost(const oracle_cfg* cfg, double alpha, double beta, int32_t links, double* seconds) {
   Cfg c;
   const int rc = load_cfg(cfg, c);
   if (rc) return rc;
+  if (links < 1) return -9;
   Emu e(c, nullptr, 1.0f, -1);
+  e.links = links;
   e.run();
-  *seconds = (double)e.steps * alpha + (double)e.step_max_sum * (double)c.esize() * beta;
+  *seconds = (double)e.steps * alpha + (double)e.step_load_sum * (double)c.esize() * beta;
   return 0;
 }
 

@@ -89,9 +89,13 @@ def test_cost_model_matches_oracle(ddl, case):
     plan, cfg = _pair(**case)
     with plan:
         for a, b in [(0.0, 1e-9), (2e-6, 0.0), (3e-6, 1.6e-10)]:
-            assert plan.cost(a, b) == pytest.approx(oracle.cost(cfg, a, b), rel=1e-12, abs=1e-18)
+            for links in (1, 2, 3, 8):
+                assert plan.cost(a, b, links) == pytest.approx(oracle.cost(cfg, a, b, links), rel=1e-12,
+                                                               abs=1e-18), links
         with pytest.raises(ddl.DDLError):
             plan.cost(-1.0, 0.0)
+        with pytest.raises(ddl.DDLError):
+            plan.cost(1.0, 0.0, 0)
 
 
 @pytest.mark.parametrize("name", ["torus4x4_resnet50", "torus8x4_resnet50_f16", "multiring64_resnet101",

@@ -7,6 +7,7 @@ retyping its formula.
 """
 import itertools
 import math
+import os
 import zlib
 
 import numpy as np
@@ -14,7 +15,7 @@ import pytest
 
 import oracle
 import synth
-from golden_io import load_buckets, load_trace
+from golden_io import GOLDEN, load_buckets, load_trace
 
 TRACES = ["ring3_n7_f32.txt", "torus2x2_n8_f32.txt", "ring3_n3_f16.txt", "torus2x2_n4_f16.txt"]
 
@@ -307,8 +308,12 @@ def test_cost_model_closed_forms_and_page3_figure(oracle_lib):
     assert oracle.cost(oracle.Config(P=16, N=n), a, b) == pytest.approx(30 * (a + n / 16 * 4 * b))
     assert oracle.cost(oracle.Config(P=16, N=n, topo="torus", X=4, Y=4), a, b) == \
         pytest.approx(6 * (a + n / 4 * 4 * b) + 6 * (a + n / 16 * 4 * b))
-    assert oracle.cost(oracle.Config(P=16, N=n, topo="multiring", k=2), a, b) == \
+    # multi-ring: one link per ring (links = k) halves the bandwidth term;
+    # one shared link keeps the ring's
+    assert oracle.cost(oracle.Config(P=16, N=n, topo="multiring", k=2), a, b, links=2) == \
         pytest.approx(30 * (a + n / 32 * 4 * b))
+    assert oracle.cost(oracle.Config(P=16, N=n, topo="multiring", k=2), a, b, links=1) == \
+        pytest.approx(30 * (a + n / 16 * 4 * b))
     # fp16 halves the bandwidth term
     assert oracle.cost(oracle.Config(P=8, N=n, dtype="f16"), 0.0, b) == pytest.approx(14 * n / 8 * 2 * b)
     # the torus keeps the ring's bandwidth term, 2(X-1)/X + 2(Y-1)/XY = 2(P-1)/P
@@ -318,6 +323,31 @@ def test_cost_model_closed_forms_and_page3_figure(oracle_lib):
     assert oracle.cost(torus, 0.0, b) == pytest.approx(oracle.cost(ring, 0.0, b))
     assert oracle.cost(torus, 1e-3, 0.0) == pytest.approx(12e-3)
     assert oracle.cost(ring, 1e-3, 0.0) == pytest.approx(30e-3)
+    # ring and torus send one message per worker per step: extra links change nothing
+    assert oracle.cost(ring, a, b, links=4) == oracle.cost(ring, a, b, links=1)
+    assert oracle.cost(torus, a, b, links=4) == oracle.cost(torus, a, b, links=1)
+    with pytest.raises(Exception):
+        oracle.cost(ring, a, b, links=0)
+
+
+def _load_cost_cases():
+    out = []
+    with open(os.path.join(GOLDEN, "cost_multiring4_k2_n10.txt")) as fh:
+        for line in fh:
+            tok = line.split()
+            if tok and tok[0] == "case":
+                out.append((tok[2], int(tok[3]), int(tok[4]), int(tok[5]), int(tok[6])))
+    return out
+
+
+@pytest.mark.parametrize("topo,k,links,steps,elems", _load_cost_cases())
+def test_cost_model_hand_worked_shared_link(oracle_lib, topo, k, links, steps, elems):
+    """The P = 4, k = 2 multi-ring of tests/golden/cost_multiring4_k2_n10.txt,
+    worked out by hand: with one link per worker a step costs its busiest
+    worker's summed messages, with a link per ring its largest message."""
+    cfg = oracle.Config(P=4, N=10, topo=topo, k=k)
+    assert oracle.cost(cfg, 1.0, 0.0, links=links) == steps
+    assert oracle.cost(cfg, 0.0, 1.0, links=links) == elems * 4
 
 
 # --------------------------------------------------------------------------

@@ -54,7 +54,9 @@ def test_random_problem_tables_match_oracle(seed):
     with ddl.Plan(**kw) as plan:
         assert plan.buckets() == oracle.buckets(cfg)
         assert plan.traffic() == oracle.traffic(cfg)
-        assert plan.cost(3e-6, 1e-10) == pytest.approx(oracle.cost(cfg, 3e-6, 1e-10), rel=1e-12, abs=1e-18)
+        links = int(rng.integers(1, 5))
+        assert plan.cost(3e-6, 1e-10, links) == pytest.approx(oracle.cost(cfg, 3e-6, 1e-10, links), rel=1e-12,
+                                                              abs=1e-18)
         for i in range(0, kw["N"], max(1, kw["N"] // 300)):
             o, inner, groups = oracle.fold_order(cfg, i)
             got = plan.fold_order(i)
