@@ -35,4 +35,21 @@ def test_reference_arm_on_an_n_d_torus_sample():
                        capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     d = json.loads([l for l in r.stdout.splitlines() if l.strip()][-1])
-    assert d["config"]["schedule"] == "torus 4x4x4" and d["value"] > 0
+    assert d["config"]["schedules"] == ["torus 4x4x4"] and d["value"] > 0
+
+
+def test_reference_arm_default_is_the_three_schedule_sweep():
+    """With no --workload the reference arm times the same step as the GPU
+    arm: ring, multi-ring k=2 and 4x4 torus on the 300M-parameter language
+    model's P=16 problem (here cut to 20,000 elements per rank), and states
+    the host cores it ran on."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--elems", "20000",
+                        "--steps", "2", "--warmup", "3"], capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([l for l in r.stdout.splitlines() if l.strip()][-1])
+    assert d["config"]["workload"] == "lm300m_sweep"
+    assert d["config"]["schedules"] == ["ring", "multi-ring k=2", "torus 4x4"]
+    assert d["config"]["P"] == 16 and d["config"]["sample_elems_per_rank"] == 20000
+    cb = d["cpu_baseline"]
+    assert cb["cores"] == 1 and cb["nproc"] >= 1 and cb["cpu_model"]
