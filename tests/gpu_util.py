@@ -82,3 +82,32 @@ def edge_samples(w):
             if 0 <= e + d < w.N:
                 out.add(e + d)
     return np.array(sorted(out), dtype=np.int64)
+
+
+def rankorder_margins(host, got_bits, scale, dtype):
+    """Error of a rank-order result against the binary64 sum of the stored
+    inputs (times the scale), normwise and element by element.
+
+    host: P arrays of stored inputs (float32, or uint16 binary16 bits) at the
+    elements of got_bits (the result in storage form).  Element-wise bound:
+    the left fold of P binary32 values is within gamma_{P-1} * sum|x| of the
+    exact sum (gamma_n = n u / (1 - n u), u = 2^-24; recursive summation,
+    Higham, Accuracy and Stability of Numerical Algorithms, ch. 4); the
+    multiply by the scale adds one rounding (u |result|); the binary64
+    reference itself is within P 2^-53 sum|x|; for binary16 storage the result
+    is rounded once more, by at most 2^-11 of its magnitude (2^-25 absolute
+    below the binary16 normal range).  Returns (normwise relative error,
+    largest element-wise |got - ref64| / bound)."""
+    P = len(host)
+    wide = [oracle.f16_to_f32(h).astype(np.float64) if dtype == "f16" else h.astype(np.float64) for h in host]
+    ref = oracle.ref64(host, scale, dtype)
+    got = (oracle.f16_to_f32(got_bits) if dtype == "f16" else got_bits).astype(np.float64)
+    abs_sum = np.abs(np.stack(wide)).sum(axis=0) * abs(float(scale))
+    u = 2.0 ** -24
+    gamma = (P - 1) * u / (1 - (P - 1) * u)
+    bound = gamma * abs_sum + u * (np.abs(ref) + gamma * abs_sum) + P * 2.0 ** -52 * abs_sum + 2.0 ** -149
+    if dtype == "f16":
+        bound = bound + np.maximum(2.0 ** -11 * (np.abs(ref) + bound), 2.0 ** -25)
+    err = np.abs(got - ref)
+    norm = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    return norm, float(np.max(err / bound))
