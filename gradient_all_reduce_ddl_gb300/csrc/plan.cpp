@@ -41,111 +41,106 @@ int gcd_int(int a, int b) {
   return a;
 }
 
-void make_buckets(const Spec& s, std::vector<Bucket>* out) {
-  out->clear();
-  auto push = [&](uint64_t lo, uint64_t hi) {
-    Bucket b{};
-    b.lo = lo;
-    b.hi = hi;
-    out->push_back(b);
-  };
-  if (s.bucket_bytes == 0) {
-    push(0, s.N);
-    return;
-  }
-  if (s.layers.empty()) {
+// The buckets of s from the highest addresses down: f(lo, hi) for each, in
+// issue order; a false return stops the walk (and is returned).
+template <typename F>
+bool for_each_bucket(const Shape& s, F&& f) {
+  if (s.bucket_bytes == 0) return f(uint64_t(0), s.N);
+  if (s.n_layers == 0) {
     const uint64_t per = s.bucket_bytes / (uint64_t)s.esize;
-    uint64_t hi = s.N;
-    while (hi > 0) {
+    for (uint64_t hi = s.N; hi > 0;) {
       const uint64_t lo = hi > per ? hi - per : 0;
-      push(lo, hi);
+      if (!f(lo, hi)) return false;
       hi = lo;
     }
-    return;
+    return true;
   }
   // tensors sit in forward order at increasing addresses; walk them backwards
   uint64_t top = s.N, cursor = s.N, bytes = 0;
-  for (size_t i = s.layers.size(); i-- > 0;) {
+  for (uint64_t i = s.n_layers; i-- > 0;) {
     cursor -= s.layers[i];
     bytes += s.layers[i] * (uint64_t)s.esize;
     if (bytes >= s.bucket_bytes) {
-      push(cursor, top);
+      if (!f(cursor, top)) return false;
       top = cursor;
       bytes = 0;
     }
   }
-  if (top > 0) push(0, top);
+  if (top > 0) return f(uint64_t(0), top);
+  return true;
 }
 
-struct Builder {
-  const Spec& s;
-  Tables* t;
-  bool with_steps;
-  std::vector<int> mult;
-  // cost model: links per worker; the elements each (worker, link) pair
-  // sends in the step being built; their maximum summed over the steps
-  int links = 1;
-  std::vector<uint64_t> load;
-  uint64_t busiest_sum = 0;
+void make_buckets(const Shape& s, std::vector<Bucket>* out) {
+  out->clear();
+  for_each_bucket(s, [&](uint64_t lo, uint64_t hi) {
+    Bucket b{};
+    b.lo = lo;
+    b.hi = hi;
+    out->push_back(b);
+    return true;
+  });
+}
 
-  void add_segment(uint64_t lo, uint64_t len, const std::vector<int>& order, int inner, int groups) {
-    if (len == 0) return;
-    Segment g;
-    g.order_off = (uint32_t)t->orders.size();
-    g.inner = (uint16_t)inner;
-    g.groups = (uint16_t)groups;
-    for (int r : order) t->orders.push_back((uint8_t)r);
-    const uint32_t seg = (uint32_t)t->segs.size();
-    t->segs.push_back(g);
+// The fused tables of one plan shape, handed to a sink; fixed-size arrays
+// only, so the allocation-free entry point can run it.
+struct FusedWalk {
+  const Shape& s;
+  FusedSink* sink;
+  int mult[kMaxP];
+  int order[kMaxP];
+
+  bool segment(uint64_t lo, uint64_t len, int inner, int groups) {
+    if (len == 0) return true;
+    if (!sink->segment(order, s.P, inner, groups)) return false;
     const uint64_t tile = (uint64_t)s.tile_bytes / (uint64_t)s.esize;
     for (uint64_t a = lo, end = lo + len; a < end;) {
       const uint64_t next = std::min(end, (a / tile + 1) * tile);
-      t->items.push_back(Item{a, (uint32_t)(next - a), seg});
+      if (!sink->item(a, (uint32_t)(next - a))) return false;
       a = next;
     }
+    return true;
   }
 
-  void fused_bucket(const Bucket& b) {
+  bool bucket(uint64_t lo, uint64_t hi) {
     const int P = s.P;
-    const uint64_t n = b.hi - b.lo;
-    std::vector<int> order(P);
+    const uint64_t n = hi - lo;
     if (s.mode == kRankOrder) {
-      std::iota(order.begin(), order.end(), 0);
-      add_segment(b.lo, n, order, P, 1);
-      return;
+      for (int t = 0; t < P; ++t) order[t] = t;
+      return segment(lo, n, P, 1);
     }
     if (s.topo == kRing || s.topo == kMultiRing) {
       const int k = s.topo == kRing ? 1 : s.k;
       for (int j = 0; j < k; ++j) {
-        const uint64_t slo = b.lo + part_lo(n, k, j), sn = part_len(n, k, j);
+        const uint64_t slo = lo + part_lo(n, k, j), sn = part_len(n, k, j);
         const int m = s.topo == kRing ? 1 : mult[j];
         for (int c = 0; c < P; ++c) {
-          for (int t2 = 0; t2 < P; ++t2) order[t2] = (int)((int64_t)((c + t2) % P) * m % P);
-          add_segment(slo + part_lo(sn, P, c), part_len(sn, P, c), order, P, 1);
+          for (int t = 0; t < P; ++t) order[t] = (int)((int64_t)((c + t) % P) * m % P);
+          if (!segment(slo + part_lo(sn, P, c), part_len(sn, P, c), P, 1)) return false;
         }
       }
-      return;
+      return true;
     }
     if (s.topo == kTorusND) {
-      nd_segments(b.lo, n, 0, std::vector<int>(s.dims.size(), 0), order);
-      return;
+      int ch[kMaxDims] = {0, 0, 0, 0};
+      return nd(lo, n, 0, ch);
     }
     const int X = s.X, Y = s.Y;
     for (int c = 0; c < X; ++c) {
-      const uint64_t clo = b.lo + part_lo(n, X, c), cn = part_len(n, X, c);
+      const uint64_t clo = lo + part_lo(n, X, c), cn = part_len(n, X, c);
       for (int d = 0; d < Y; ++d) {
         for (int g = 0; g < Y; ++g)
           for (int h = 0; h < X; ++h) order[g * X + h] = ((d + g) % Y) * X + (c + h) % X;
-        add_segment(clo + part_lo(cn, Y, d), part_len(cn, Y, d), order, X, Y);
+        if (!segment(clo + part_lo(cn, Y, d), part_len(cn, Y, d), X, Y)) return false;
       }
     }
+    return true;
   }
 
   // n-D torus: the range [lo, lo+n) is split along dim k into D_k chunks;
   // chunk tuple (c_0..c_{d-1}) folds, innermost first, the ranks with
   // coordinates x_k = (c_k + g_k) mod D_k for g_k = 0..D_k-1.
-  void nd_segments(uint64_t lo, uint64_t n, int k, std::vector<int> ch, std::vector<int>& order) {
-    const int d = (int)s.dims.size();
+  bool nd(uint64_t lo, uint64_t n, int k, int* ch) {
+    const int d = s.ndims;
     if (k == d) {
       for (int t = 0; t < s.P; ++t) {
         int rest = t, r = 0, stride = 1;
@@ -157,14 +152,58 @@ struct Builder {
         }
         order[t] = r;
       }
-      add_segment(lo, n, order, s.dims[0], s.P / s.dims[0]);
-      return;
+      return segment(lo, n, s.dims[0], s.P / s.dims[0]);
     }
+    if (k >= kMaxDims) return false;  // check_shape keeps ndims <= kMaxDims
     for (int c = 0; c < s.dims[k]; ++c) {
       ch[k] = c;
-      nd_segments(lo + part_lo(n, s.dims[k], c), part_len(n, s.dims[k], c), k + 1, ch, order);
+      if (!nd(lo + part_lo(n, s.dims[k], c), part_len(n, s.dims[k], c), k + 1, ch)) return false;
     }
+    return true;
   }
+};
+
+// The plan's tables, filled from the walk.
+struct TableSink final : FusedSink {
+  Tables* t;
+  size_t b = 0;
+  explicit TableSink(Tables* tab) : t(tab) {}
+  bool bucket(uint64_t lo, uint64_t hi) override {
+    if (b >= t->buckets.size() || t->buckets[b].lo != lo || t->buckets[b].hi != hi) return false;
+    t->buckets[b].item_begin = (uint32_t)t->items.size();
+    return true;
+  }
+  bool bucket_end() override {
+    t->buckets[b++].item_end = (uint32_t)t->items.size();
+    return true;
+  }
+  bool segment(const int* order, int P, int inner, int groups) override {
+    Segment g;
+    g.order_off = (uint32_t)t->orders.size();
+    g.inner = (uint16_t)inner;
+    g.groups = (uint16_t)groups;
+    for (int r = 0; r < P; ++r) t->orders.push_back((uint8_t)order[r]);
+    t->segs.push_back(g);
+    return true;
+  }
+  bool item(uint64_t begin, uint32_t len) override {
+    t->items.push_back(Item{begin, len, (uint32_t)(t->segs.size() - 1)});
+    return true;
+  }
+};
+
+// The step-by-step schedule: message lists (stepwise mode), traffic, steps
+// and the cost model.
+struct Builder {
+  const Spec& s;
+  Tables* t;
+  bool with_steps;
+  std::vector<int> mult;
+  // cost model: links per worker; the elements each (worker, link) pair
+  // sends in the step being built; their maximum summed over the steps
+  int links = 1;
+  std::vector<uint64_t> load;
+  uint64_t busiest_sum = 0;
 
   // ---- message lists of the step-by-step schedule ----
   std::vector<Xfer> cur;
@@ -348,18 +387,47 @@ uint32_t bulk_tile_bytes(int P) {
   return t;
 }
 
-bool ring_multipliers(int P, int k, std::vector<int>* out) {
-  out->clear();
+bool ring_multipliers_into(int P, int k, int* out) {
   if (P == 1) {
-    out->push_back(1);
+    out[0] = 1;
     return k == 1;
   }
-  for (int c = 1; c < P && (int)out->size() < k; ++c)
-    if (gcd_int(c, P) == 1) out->push_back(c);
-  return (int)out->size() == k;
+  int found = 0;
+  for (int c = 1; c < P && found < k; ++c)
+    if (gcd_int(c, P) == 1) out[found++] = c;
+  return found == k;
 }
 
-std::string validate(const Spec& s, bool* unsupported) {
+bool ring_multipliers(int P, int k, std::vector<int>* out) {
+  out->clear();
+  if (P < 1 || P > kMaxP || k < 1) return false;
+  int m[kMaxP];
+  const bool ok = ring_multipliers_into(P, k, m);
+  const int n = P == 1 ? 1 : std::min(k, P - 1);
+  out->assign(m, m + std::min(n, k));
+  return ok;
+}
+
+Shape shape_of(const Spec& s) {
+  Shape h;
+  h.P = s.P;
+  h.N = s.N;
+  h.esize = s.esize;
+  h.topo = s.topo;
+  h.k = s.k;
+  h.X = s.X;
+  h.Y = s.Y;
+  h.bucket_bytes = s.bucket_bytes;
+  h.layers = s.layers.empty() ? nullptr : s.layers.data();
+  h.n_layers = s.layers.size();
+  h.mode = s.mode;
+  h.tile_bytes = s.tile_bytes;
+  h.ndims = (int)s.dims.size();
+  for (int d = 0; d < kMaxDims && d < h.ndims; ++d) h.dims[d] = s.dims[d];
+  return h;
+}
+
+const char* check_shape(const Shape& s, bool* unsupported) {
   *unsupported = false;
   if (s.P < 1) return "P must be >= 1";
   if (s.P > kMaxP) {
@@ -370,53 +438,80 @@ std::string validate(const Spec& s, bool* unsupported) {
   if (s.esize != 4 && s.esize != 2) return "dtype must be DDL_FP32 or DDL_FP16";
   if (s.mode < kFused || s.mode > kRankOrder) return "unknown mode";
   if (s.topo == kMultiRing) {
-    std::vector<int> m;
+    int m[kMaxP];
     if (s.k < 1) return "multi-ring needs k >= 1";
-    if (!ring_multipliers(s.P, s.k, &m)) {
+    if (!ring_multipliers_into(s.P, s.k, m)) {
       *unsupported = true;
       return "multi-ring k exceeds the number of distinct rank orders t*s mod P (phi(P))";
     }
   } else if (s.topo == kTorus) {
     if (s.X < 1 || s.Y < 1 || (int64_t)s.X * s.Y != s.P) return "torus needs X * Y == P";
   } else if (s.topo == kTorusND) {
-    if (s.dims.empty() || (int)s.dims.size() > kMaxDims) return "n-D torus needs 1..4 dims";
+    if (s.ndims < 1 || s.ndims > kMaxDims) return "n-D torus needs 1..4 dims";
     int64_t prod = 1;
-    for (int d : s.dims) {
-      if (d < 1) return "n-D torus dims must be >= 1";
-      prod *= d;
+    for (int d = 0; d < s.ndims; ++d) {
+      if (s.dims[d] < 1) return "n-D torus dims must be >= 1";
+      prod *= s.dims[d];
     }
     if (prod != s.P) return "n-D torus dims must multiply to P";
-    if (s.dims.size() > 1 && s.dims.back() == 1) return "trailing dims of size 1 must be dropped";
+    if (s.ndims > 1 && s.dims[s.ndims - 1] == 1) return "trailing dims of size 1 must be dropped";
   } else if (s.topo != kRing) {
     return "unknown topology kind";
   }
   if (s.bucket_bytes != 0 && s.bucket_bytes < (uint64_t)s.esize) return "bucket_bytes smaller than one element";
-  if (!s.layers.empty()) {
+  if (s.n_layers > 0) {
+    if (!s.layers) return "layer list missing";
     uint64_t sum = 0;
-    for (uint64_t v : s.layers) {
+    for (uint64_t i = 0; i < s.n_layers; ++i) {
+      const uint64_t v = s.layers[i];
       if (v == 0) return "a layer has zero elements";
+      if (v > s.N - sum) return "layer sizes exceed N";  // also keeps the sum from wrapping
       sum += v;
     }
     if (sum != s.N) return "layer sizes do not sum to N";
   }
-  // work-item indices are 32-bit: up to 2^40 bytes per rank
-  if (s.N * (uint64_t)s.esize > (1ull << 40)) {
+  // work-item indices are 32-bit: up to 2^40 bytes per rank (compared
+  // without forming N * esize, which could wrap)
+  if (s.N > (1ull << 40) / (uint64_t)s.esize) {
     *unsupported = true;
     return "more than 2^40 bytes per rank";
   }
-  return "";
+  if (s.tile_bytes < (uint32_t)s.esize || s.tile_bytes % (uint32_t)s.esize) return "bad tile size";
+  return nullptr;
+}
+
+std::string validate(const Spec& s, bool* unsupported) {
+  if ((size_t)s.dims.size() > (size_t)kMaxDims) {
+    *unsupported = false;
+    return "n-D torus needs 1..4 dims";
+  }
+  const char* why = check_shape(shape_of(s), unsupported);
+  return why ? std::string(why) : std::string();
+}
+
+bool emit_fused(const Shape& s, FusedSink* sink) {
+  FusedWalk walk{s, sink, {}, {}};
+  if (s.topo == kMultiRing && !ring_multipliers_into(s.P, s.k, walk.mult)) return false;
+  return for_each_bucket(s, [&](uint64_t lo, uint64_t hi) {
+    return sink->bucket(lo, hi) && walk.bucket(lo, hi) && sink->bucket_end();
+  });
 }
 
 bool build_tables(const Spec& s, bool with_steps, Tables* t) {
   try {
     *t = Tables();
-    make_buckets(s, &t->buckets);
+    const Shape sh = shape_of(s);
+    make_buckets(sh, &t->buckets);
+    if (s.mode != kStepwise) {
+      TableSink sink(t);
+      if (!emit_fused(sh, &sink)) {
+        *t = Tables();
+        return false;
+      }
+    }
     Builder bld{s, t, with_steps, {}};
     if (s.topo == kMultiRing) ring_multipliers(s.P, s.k, &bld.mult);
     for (Bucket& b : t->buckets) {
-      b.item_begin = (uint32_t)t->items.size();
-      if (s.mode != kStepwise) bld.fused_bucket(b);
-      b.item_end = (uint32_t)t->items.size();
       b.step_begin = (uint32_t)t->steps.size();
       bld.step_bucket(b);
       b.step_end = (uint32_t)t->steps.size();
@@ -434,7 +529,7 @@ bool build_tables(const Spec& s, bool with_steps, Tables* t) {
 bool schedule_cost(const Spec& s, double alpha, double beta, int links, double* seconds) {
   try {
     Tables t;
-    make_buckets(s, &t.buckets);
+    make_buckets(shape_of(s), &t.buckets);
     Builder bld{s, &t, false, {}};
     // more links than concurrent rings carry nothing
     bld.links = std::max(1, std::min(links, s.topo == kMultiRing ? s.k : 1));

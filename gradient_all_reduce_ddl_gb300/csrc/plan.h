@@ -97,11 +97,55 @@ struct Tables {
   uint64_t nsteps = 0;  // sequential communication steps
 };
 
-// Returns "" if the spec is valid, else a reason.  unsupported is set when the
-// request is valid in principle but outside what this library builds.
+// What fixes the fused tables, as plain values that own no memory (the
+// allocation-free entry point builds one without touching the heap).
+struct Shape {
+  int P = 0;
+  uint64_t N = 0;
+  int esize = 4;
+  int topo = kRing;
+  int k = 1, X = 0, Y = 0;
+  uint64_t bucket_bytes = 0;
+  const uint64_t* layers = nullptr;  // tensor sizes in forward order, or null
+  uint64_t n_layers = 0;
+  int mode = kFused;
+  uint32_t tile_bytes = kTileBytes;
+  int ndims = 0;
+  int dims[kMaxDims] = {0, 0, 0, 0};
+};
+
+Shape shape_of(const Spec& s);
+
+// Receives the fused (or rank-order) tables in table order: for every bucket
+// (highest addresses first) its segments, and after each segment its work
+// items.  A false return stops the walk.
+struct FusedSink {
+  virtual bool bucket(uint64_t lo, uint64_t hi) = 0;
+  virtual bool segment(const int* order, int P, int inner, int groups) = 0;
+  virtual bool item(uint64_t begin, uint32_t len) = 0;
+  virtual bool bucket_end() { return true; }
+
+ protected:
+  ~FusedSink() = default;
+};
+
+// Walks the fused tables of s into the sink; uses no heap memory.  Returns
+// false if the sink stopped the walk.  Items never cross a segment edge or a
+// tile_bytes-aligned boundary.
+bool emit_fused(const Shape& s, FusedSink* sink);
+
+// nullptr if the shape is valid, else a static reason.  *unsupported is set
+// when the request is valid in principle but outside what this library
+// builds.  Uses no heap memory.
+const char* check_shape(const Shape& s, bool* unsupported);
+
+// Returns "" if the spec is valid, else a reason (check_shape on the spec).
 std::string validate(const Spec& s, bool* unsupported);
 
-// The multi-ring multipliers s_0..s_{k-1}; false if fewer than k exist.
+// The multi-ring multipliers s_0..s_{k-1} (the j-th smallest integers in
+// [1, P) coprime to P; s_0 = 1 when P = 1) into out[0..k-1]; false if fewer
+// than k exist.  No heap memory.
+bool ring_multipliers_into(int P, int k, int* out);
 bool ring_multipliers(int P, int k, std::vector<int>* out);
 
 // Builds buckets, the fused (or rank-order) segment and item tables, and the

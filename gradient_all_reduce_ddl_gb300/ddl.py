@@ -39,7 +39,7 @@ EXPORTS = [
     "ddl_plan_num_buckets", "ddl_plan_bucket_range", "ddl_plan_traffic", "ddl_plan_fold_order",
     "ddl_plan_launches", "ddl_plan_check", "ddl_status_string", "ddl_plan_destroy", "ddl_allreduce_noalloc",
     "ddl_plan_cost", "ddl_plan_set_torus_dims", "ddl_allreduce_sgd", "ddl_selftest_wait_timeout",
-    "ddl_allreduce_slab",
+    "ddl_allreduce_slab", "ddl_noalloc_check",
 ]
 
 
@@ -82,6 +82,7 @@ _sig("ddl_selftest_wait_timeout", _i, _vp, ctypes.c_uint32, _vp)
 _sig("ddl_status_string", ctypes.c_char_p, _i)
 _sig("ddl_plan_destroy", _i, _vp)
 _sig("ddl_allreduce_noalloc", _i, _i, _sz, _i, ddl_topology_t, _sz, _i, _P(_sz), _P(_vp), _f, _vp)
+_sig("ddl_noalloc_check", _i, _vp)
 
 
 class DDLError(RuntimeError):
@@ -252,6 +253,12 @@ def ddl_allreduce_noalloc(P, N, dtype, topology, bucket_bytes, layers, rank_bufs
     _ok(_lib.ddl_allreduce_noalloc(P, N, dtype, topology, bucket_bytes, len(layers), arr,
                                    _ptr_array(_dev_ptrs(rank_bufs)), scale, _stream_handle(stream)),
         "ddl_allreduce_noalloc")
+
+
+def ddl_noalloc_check(stream=None):
+    """Status of the last allocation-free call's kernel on the current device
+    (waits for `stream`); DDL_ERR_DEVICE_CHECK raises."""
+    _ok(_lib.ddl_noalloc_check(_stream_handle(stream)), "ddl_noalloc_check")
 
 
 # -- convenience object --------------------------------------------------------

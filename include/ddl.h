@@ -104,7 +104,15 @@ typedef enum {
 
 typedef struct ddl_plan* ddl_plan_t;
 
-/* Creates a plan for P rank buffers of N elements each.
+/* Creates a plan for P rank buffers of N elements each: the averaging step
+ * of synchronous data-parallel SGD, in which every worker holds a full copy
+ * of the gradient and all of them end with the same mean (Baidu
+ * ring-allreduce write-up, final page, opening paragraphs and "总结"; Sony
+ * page, "2大方法解决不稳定问题").  topo picks the schedule: the ring
+ * (Baidu write-up, "总结"), the multi-ring ("[论文解读] PowerAI DDL",
+ * ABSTRACT and "提出的方法") or the 2D torus (Sony page, "2D-Torus
+ * All-reduce", Fig. 1 and Fig. 2); dtype DDL_FP16 is the half-precision
+ * gradient communication of the Sony page, "训练设置".
  *  P: 1..256.  N: >= 1 elements per rank.
  *  bucket_bytes: 0 = the whole buffer is one bucket; otherwise buckets of at
  *    least this many bytes, taken from the highest addresses down (bucket 0 =
@@ -141,7 +149,15 @@ ddl_status_t ddl_plan_set_layers(ddl_plan_t plan, int n_tensors, const size_t* n
  * DDL_TORUS result and dims {P} the ring's.  Host-only. */
 ddl_status_t ddl_plan_set_torus_dims(ddl_plan_t plan, int ndims, const int* dims);
 
-/* Selects the mode (default DDL_MODE_FUSED).  Host-only. */
+/* Selects the mode (default DDL_MODE_FUSED).  DDL_MODE_FUSED and
+ * DDL_MODE_STEPWISE give the bits of the schedule run send by send (the ring
+ * of the Baidu write-up, "总结"; the torus of the Sony page, "2D-Torus
+ * All-reduce"; fp16 hops of its "训练设置"): the first in one HBM pass, the
+ * second with one kernel per communication step.  DDL_MODE_RANKORDER adds
+ * the ranks in plain order 0..P-1, which the pages do not describe; it is
+ * the reordered fast mode, accurate to the binary64 sum within 1e-6 (fp32)
+ * or 2e-3 (fp16) normwise and within the error bound of a P-term binary32
+ * sum element by element.  Host-only. */
 ddl_status_t ddl_plan_set_mode(ddl_plan_t plan, ddl_mode_t mode);
 
 /* Selects the fused kernel variant (default DDL_KERNEL_AUTO).  Results are
@@ -243,35 +259,52 @@ ddl_status_t ddl_overlap_end(ddl_plan_t plan, void* stream);
  * a training loop that must not take cudaMalloc's implicit device
  * synchronisation, or a deployment that fixes its memory footprint at
  * start-up.  The arguments mean what they mean for ddl_plan_create,
- * ddl_plan_set_layers (n_tensors = 0: no layer list) and ddl_allreduce; the
- * mode is DDL_MODE_FUSED and the results are bit-identical to a plan's.
+ * ddl_plan_set_layers (n_tensors = 0: no layer list) and ddl_allreduce
+ * (topo.kind DDL_RING, DDL_MULTIRING or DDL_TORUS); the mode is
+ * DDL_MODE_FUSED and the results are bit-identical to a plan's, whose table
+ * code it runs.
  *  - The fused kernel's work tables live in one static 1 MiB device array
  *    inside this library (every GPU that loads it holds the array until the
  *    process exits) instead of plan-owned device memory.  Problems whose
  *    tables need more than that (about 60,000 tiles of 8 KB per rank, i.e.
  *    roughly 480 MB per rank) return DDL_ERR_UNSUPPORTED before any work.
  *  - No cudaMalloc, cudaFree or other allocating call, and no host heap use.
- *    The tables are copied from a static host buffer with cudaMemcpyAsync
- *    from pageable memory, so the call waits for earlier work on `stream`.
+ *    The tables are written into a static host buffer and copied into the
+ *    array with cudaMemcpyAsync on `stream`, ordered before the kernel; the
+ *    call returns once the runtime holds its own copy of the host buffer.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    before any stream capture.
  *  - All calls share the array, which keeps the last call's tables; each call
- *    rewrites what it uses and clears the kernel error word.  Calls whose GPU
- *    work overlaps (other streams, other host threads) race on the array and
- *    must be ordered by the caller.  Host threads are serialised inside. */
+ *    rewrites what it uses and clears the kernel error word (read it with
+ *    ddl_noalloc_check).  Calls whose GPU work overlaps (other streams, other
+ *    host threads) race on the array and must be ordered by the caller.  Host
+ *    threads are serialised inside. */
 ddl_status_t ddl_allreduce_noalloc(int P, size_t N, ddl_dtype_t dtype, ddl_topology_t topo, size_t bucket_bytes,
                                    int n_tensors, const size_t* numel_fwd_order, void* const* rank_bufs,
                                    float scale, void* stream);
+
+/* Reads the kernel error word that the last ddl_allreduce_noalloc on the
+ * current device left in the static array, without allocating: waits for
+ * `stream` (the stream of that call), copies the word into a static host
+ * word, and returns DDL_ERR_DEVICE_CHECK if the kernel found a bad table
+ * entry (the word is then cleared), DDL_OK otherwise or when no
+ * allocation-free call has run on this device.  The web pages have no
+ * counterpart. */
+ddl_status_t ddl_noalloc_check(void* stream);
 
 /* Bucket table: *n buckets; bucket b covers elements [*begin, *end). */
 ddl_status_t ddl_plan_num_buckets(ddl_plan_t plan, int* n);
 ddl_status_t ddl_plan_bucket_range(ddl_plan_t plan, int bucket, size_t* begin, size_t* end);
 
 /* What the schedule would move between workers: the total number of
- * elements sent over all messages (2(P-1)N for every schedule) and the number
- * of sequential communication steps (ring and multi-ring 2(P-1), torus
- * 2(X-1)+2(Y-1), per bucket).  Host-only. */
+ * elements sent over all messages (2(P-1)N for every schedule, so each
+ * worker sends and receives 2(P-1)/P of the gradient: the Baidu write-up's
+ * "each GPU sends and receives about 2.4 GB" for a 1.2 GB gradient, final
+ * page, opening paragraphs) and the number of sequential communication steps
+ * (ring and multi-ring 2(P-1), torus 2(X-1)+2(Y-1), per bucket; the torus's
+ * fewer steps are the point of the Sony page's "2D-Torus All-reduce").
+ * Host-only. */
 ddl_status_t ddl_plan_traffic(ddl_plan_t plan, uint64_t* elems_moved_total, uint64_t* steps);
 
 /* alpha-beta cost of the schedule on a cluster of P real workers, each with

@@ -206,3 +206,34 @@ def test_kernel_choice_range(ddl):
             assert ddl._lib.ddl_plan_set_kernel(plan.handle, k) == ddl.DDL_OK, k
         assert ddl._lib.ddl_plan_set_kernel(plan.handle, 6) == ddl.DDL_ERR_INVALID_ARG
         assert ddl._lib.ddl_plan_set_kernel(plan.handle, -1) == ddl.DDL_ERR_INVALID_ARG
+
+
+def test_layer_sizes_that_would_wrap_are_refused(ddl):
+    """A layer list whose sum wraps around 2^64 to N is not a partition of N."""
+    with ddl.Plan(3, 1) as plan:
+        with pytest.raises(ddl.DDLError) as ei:
+            ddl.ddl_plan_set_layers(plan.handle, [2 ** 64 - 1, 2])
+        assert ei.value.status == ddl.DDL_ERR_INVALID_ARG
+        assert plan.buckets() == [(0, 1)]
+
+
+def test_noalloc_refuses_oversized_problems_before_any_gpu_work(ddl):
+    """Sizes are checked without forming N * element size (which could wrap),
+    and the table count stops at the first table that no longer fits the
+    static array: both refusals come back at once, before any CUDA call."""
+    import time
+    ring = ddl.ddl_topology_t(ddl.DDL_RING, 1, 0, 0)
+    fake = [1 << 30, 2 << 30]
+    for N in (2 ** 62 + 1, 2 ** 63 + 7):     # N * 4 wraps to a small number
+        with pytest.raises(ddl.DDLError) as ei:
+            ddl.ddl_allreduce_noalloc(2, N, ddl.DDL_FP32, ring, 0, None, fake, 0.5)
+        assert ei.value.status == ddl.DDL_ERR_UNSUPPORTED
+    t = time.perf_counter()
+    with pytest.raises(ddl.DDLError) as ei:        # 2^40 bytes per rank: ~2^27 tiles, far over 1 MiB of tables
+        ddl.ddl_allreduce_noalloc(2, 2 ** 38, ddl.DDL_FP32, ring, 4, None, fake, 0.5)
+    assert ei.value.status == ddl.DDL_ERR_UNSUPPORTED
+    assert time.perf_counter() - t < 1.0
+    torus = ddl.ddl_topology_t(3, 1, 0, 0)      # the n-D kind is not part of the topology struct
+    with pytest.raises(ddl.DDLError) as ei:
+        ddl.ddl_allreduce_noalloc(2, 100, ddl.DDL_FP32, torus, 0, None, fake, 0.5)
+    assert ei.value.status == ddl.DDL_ERR_INVALID_ARG
