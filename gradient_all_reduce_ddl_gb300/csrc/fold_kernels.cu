@@ -1363,6 +1363,10 @@ cudaError_t launch_items(void (*kernel)(FoldParams), const FoldParams& p, uint32
 
 template <bool F16>
 cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t stream, bool early) {
+  // two 16-byte columns per thread cover kTileBytes per rank; a larger item
+  // is refused (the element-wise path, taken for unaligned buffers, covers
+  // any item)
+  if (p.vector_ok && p.tile_bytes > (uint32_t)kTileBytes) return cudaErrorInvalidValue;
   if constexpr (F16) {
     if (p.round_hops)
       return launch_items(fold_ldg_kernel<true, true, 2, DDL_LDG_F16_B, DDL_LDG_MINB>, p, n_items, stream, early);

@@ -382,7 +382,9 @@ uint32_t ldg_tile_bytes(uint64_t bytes_per_rank) {
 }
 
 uint32_t bulk_tile_bytes(int P) {
-  uint32_t t = 16384;
+  // at most kTileBytes: where a staged pass does not apply, the register pass
+  // runs the same items, and its columns cover kTileBytes per rank
+  uint32_t t = kTileBytes;
   while (t > 256 && (uint64_t)t * (uint64_t)P > 65536) t >>= 1;
   return t;
 }

@@ -78,7 +78,7 @@ struct Spec {
 };
 
 // Work-item size of the shared-memory-staged pass: P ranks' tiles of one
-// pipeline stage fill about 64 KB, between 256 B and 16 KB per rank.
+// pipeline stage fill about 64 KB, between 256 B and kTileBytes per rank.
 uint32_t bulk_tile_bytes(int P);
 
 // Work-item size of the register pass: kTileBytes, or smaller (down to 1 KB)

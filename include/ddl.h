@@ -243,12 +243,17 @@ ddl_status_t ddl_allreduce_bucket(ddl_plan_t plan, int bucket, void* const* rank
 ddl_status_t ddl_allreduce_host(ddl_plan_t plan, void* const* host_bufs, void* const* dev_bufs, float scale,
                                 void* stream);
 
-/* Overlap with back-propagation.  ddl_overlap_begin records the buffers and
- * scale; each ddl_bucket_ready(b, stream) marks bucket b's gradients complete
- * at the current point of `stream` (an event), after which the plan's side
- * stream all-reduces bucket b; ddl_overlap_end makes `stream` wait for every
- * bucket issued so far.  Each bucket is signalled at most once per
- * begin/end pair; bucket 0 (output layers) is normally signalled first. */
+/* Overlap with back-propagation: the all-reduce of the output layers'
+ * gradients starts while the earlier layers' are still being computed
+ * (Baidu write-up, final page, opening paragraphs).  ddl_overlap_begin
+ * records the buffers and scale; each ddl_bucket_ready(b, stream) marks
+ * bucket b's gradients complete at the current point of `stream` (an event),
+ * after which the plan's side stream all-reduces bucket b; ddl_overlap_end
+ * makes `stream` wait for every bucket issued so far, then all-reduces on
+ * `stream` every bucket that was never signalled, so every bucket is reduced
+ * once per begin/end pair.  Each bucket is signalled at most once per
+ * begin/end pair (a second signal returns DDL_ERR_INVALID_ARG); bucket 0
+ * (output layers) is normally signalled first. */
 ddl_status_t ddl_overlap_begin(ddl_plan_t plan, void* const* rank_bufs, float scale, void* stream);
 ddl_status_t ddl_bucket_ready(ddl_plan_t plan, int bucket, void* stream);
 ddl_status_t ddl_overlap_end(ddl_plan_t plan, void* stream);

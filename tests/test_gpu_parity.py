@@ -186,6 +186,31 @@ def test_allreduce_sgd_matches_oracle(ddl, case, mom, keep):
         assert np.array_equal(to_numpy_bits(grads[r]), g_ref[r] if keep else host[r]), ("grads", r)
 
 
+@pytest.mark.parametrize("kernel", ["bulk", "bulkload", "tma", "chunked"])
+@pytest.mark.parametrize("P", [2, 4])
+def test_small_p_with_a_staged_kernel_choice(ddl, kernel, P):
+    """P <= 4 with a staged kernel chosen.  A staged tile once grew to 16 KB
+    per rank at such P, more than the register pass covers, and the register
+    pass runs those items for ddl_allreduce with the tensor-map choice and
+    for the fused SGD pass with any choice: both must match the oracle."""
+    w = _w(P=P, N=200_003, seed=77)
+    _check_exact(ddl, w, kernel=kernel)
+    host = _host_inputs(w)
+    p0 = np.linspace(-1, 1, w.N, dtype=np.float32)
+    g_ref = [h.copy() for h in host]
+    p_ref = [p0.copy() for _ in range(w.P)]
+    oracle.sgd(oracle_cfg(w), g_ref, p_ref, None, w.scale, 0.1, 0.0, 0.0)
+    grads = device_bufs_from_host(host, DEV)
+    params = [torch.from_numpy(p0).to(DEV) for _ in range(w.P)]
+    with ddl.Plan.for_workload(w, kernel=kernel) as plan:
+        plan.allreduce_sgd(grads, params, None, w.scale, 0.1)
+        torch.cuda.synchronize()
+        plan.check()
+    for r in range(w.P):
+        assert np.array_equal(to_numpy_bits(grads[r]), g_ref[r]), r
+        assert np.array_equal(params[r].cpu().numpy(), p_ref[r]), r
+
+
 def test_allreduce_sgd_unaligned_and_errors(ddl):
     w = _w(P=6, N=12_345, seed=43)
     host = _host_inputs(w)
@@ -564,6 +589,39 @@ def test_overlap_with_backward_matches_allreduce(ddl):
         assert plan.launches == nb
     for r in range(w.P):
         assert np.array_equal(to_numpy_bits(bufs[r]), ref[r])
+
+
+@pytest.mark.parametrize("signalled", [[0, 2], [], [3], [1, 2]])
+def test_overlap_end_reduces_buckets_never_signalled(ddl, signalled):
+    """ddl_overlap_end all-reduces, on the producer stream, every bucket that
+    was never signalled: the result is the oracle's whichever buckets were."""
+    w = _w(P=6, N=240_001, topo="torus", X=3, Y=2, layers=[60_000] * 3 + [60_001], bucket_bytes=200_000, seed=8)
+    host = _host_inputs(w)
+    ref = [h.copy() for h in host]
+    oracle.emulate(oracle_cfg(w), ref, w.scale)
+    bufs = [torch.zeros(w.N, dtype=torch.float32, device=DEV) for _ in range(w.P)]
+    src = device_bufs_from_host(host, DEV)
+    torch.cuda.synchronize()
+    main = torch.cuda.Stream()
+    with ddl.Plan.for_workload(w) as plan:
+        assert plan.num_buckets == 4
+        with torch.cuda.stream(main):
+            plan.overlap_begin(bufs, w.scale, stream=main)
+            for b in range(plan.num_buckets):
+                lo, hi = plan.bucket_range(b)
+                for r in range(w.P):
+                    bufs[r][lo:hi].copy_(src[r][lo:hi])
+                if b in signalled:
+                    plan.bucket_ready(b, stream=main)
+            if signalled:
+                with pytest.raises(ddl.DDLError):     # a bucket is signalled once per begin/end pair
+                    plan.bucket_ready(signalled[0], stream=main)
+            plan.overlap_end(stream=main)
+        main.synchronize()
+        torch.cuda.synchronize()
+        plan.check()
+    for r in range(w.P):
+        assert np.array_equal(to_numpy_bits(bufs[r]), ref[r]), r
 
 
 @pytest.mark.parametrize("name", ["multiring64_resnet101", "torus4x4x4_resnet101"])
