@@ -749,9 +749,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS) + sorted(SWEEPS))
     ap.add_argument("--mode", default="fused", choices=["fused", "stepwise", "rankorder"])
-    ap.add_argument("--kernel", default="auto", choices=["auto", "ldg", "bulk", "bulkload", "tma", "chunked"])
-    ap.add_argument("--slab", action="store_true",
-                    help="rank buffers in one slab (ddl_allreduce_slab); needed by --kernel tma")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "ldg", "bulkload", "chunked"])
+    ap.add_argument("--slab", action="store_true", help="rank buffers in one slab (ddl_allreduce_slab)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -885,9 +884,7 @@ def main():
     kernel_bytes = sum(kernel_bytes_of(p, w, args.mode) for p, w in zip(plans, wls))
     avg_launch_ms = local_ms / (args.steps * launches_per_step)
     achieved = (kernel_bytes / launches_per_step) / (avg_launch_ms * 1e-3) / 1e9
-    kernel_name = {"fused": {"bulk": "fold_bulk_kernel", "bulkload": "fold_bulk_kernel",
-                             "chunked": "fold_chunked_kernel",
-                             "tma": "fold_tma_kernel" if args.slab else "fold_ldg_kernel"}.get(
+    kernel_name = {"fused": {"bulkload": "fold_bulk_kernel", "chunked": "fold_chunked_kernel"}.get(
                                  args.kernel, "fold_nd_kernel" if w0.topo == "torus_nd" else "fold_ldg_kernel"),
                    "rankorder": "fold_ldg_kernel (rank order)", "stepwise": "step_kernel"}[args.mode]
     traffic = None

@@ -4,8 +4,6 @@
 // stream and the per-bucket events.  Every entry point validates its
 // arguments before queueing anything, maps CUDA failures to DDL_ERR_CUDA, and
 // never throws across the ABI.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
@@ -47,11 +45,6 @@ struct ddl_plan {
   // last parameter / momentum pointer set that passed the checks
   std::vector<void*> checked_sgd;
   bool checked_sgd_aligned = false;
-  // slab tensor map (ddl_allreduce_slab with DDL_KERNEL_TMA), kept per slab
-  CUtensorMap tmap;  // the type carries its own 64-byte alignment
-  void* tmap_base = nullptr;
-  size_t tmap_stride = 0;
-  uint32_t tmap_box = 0;
   // host-buffer pipeline: copy-in, compute and copy-out streams, events
   cudaStream_t hs[3] = {nullptr, nullptr, nullptr};
   std::vector<cudaEvent_t> hev;
@@ -148,8 +141,7 @@ uint32_t choose_tile(const Spec& s, int kernel) {
     const uint32_t cap = (s.esize == 2 && s.mode != ddl::kFused) ? 4096u : 8192u;
     return ldg < cap ? ldg : cap;
   }
-  if (kernel == DDL_KERNEL_BULK || kernel == DDL_KERNEL_BULK_LOAD || kernel == DDL_KERNEL_TMA)
-    return ddl::bulk_tile_bytes(s.P);
+  if (kernel == DDL_KERNEL_BULK_LOAD) return ddl::bulk_tile_bytes(s.P);
   return ldg;
 }
 
@@ -246,7 +238,6 @@ ddl_status_t run_items(ddl_plan* p, uint32_t ia, uint32_t ib, void* const* bufs,
   // the staged passes need 16-byte aligned buffers; otherwise the register
   // pass runs (its element-wise path), with the same results
   int variant = ddl::kVarLdg;
-  if (aligned && p->kernel == DDL_KERNEL_BULK) variant = ddl::kVarBulk;
   if (aligned && p->kernel == DDL_KERNEL_BULK_LOAD) variant = ddl::kVarBulkLoad;
   if (aligned && p->kernel == DDL_KERNEL_CHUNKED) variant = ddl::kVarChunked;
   if (aligned && force_variant) variant = force_variant;
@@ -413,7 +404,9 @@ ddl_status_t ddl_plan_set_torus_dims(ddl_plan_t p, int ndims, const int* dims) {
 }
 
 ddl_status_t ddl_plan_set_kernel(ddl_plan_t p, ddl_kernel_t k) {
-  if (!p || p->ov_active || k < DDL_KERNEL_AUTO || k > DDL_KERNEL_CHUNKED) return DDL_ERR_INVALID_ARG;
+  if (!p || p->ov_active) return DDL_ERR_INVALID_ARG;
+  if (k != DDL_KERNEL_AUTO && k != DDL_KERNEL_LDG && k != DDL_KERNEL_BULK_LOAD && k != DDL_KERNEL_CHUNKED)
+    return DDL_ERR_INVALID_ARG;
   const uint32_t tile = choose_tile(p->spec, (int)k);
   if (tile != p->spec.tile_bytes) {
     const Spec old = p->spec;
@@ -522,40 +515,6 @@ ddl_status_t ddl_allreduce_sgd(ddl_plan_t p, void* const* grad_bufs, float* cons
   return DDL_OK;
 }
 
-// Encodes the plan's tensor map over a slab: 2D, inner dim N elements, outer
-// dim P ranks at rank_stride bytes; boxes of box_elems x P.
-static ddl_status_t encode_slab_map(ddl_plan* p, void* base, size_t stride, uint32_t box) {
-  if (p->tmap_base == base && p->tmap_stride == stride && p->tmap_box == box) return DDL_OK;
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn) {
-      cudaGetLastError();
-      return DDL_ERR_CUDA;
-    }
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
-  const cuuint64_t dims[2] = {(cuuint64_t)p->spec.N, (cuuint64_t)p->spec.P};
-  const cuuint64_t strides[1] = {(cuuint64_t)stride};
-  const cuuint32_t boxdim[2] = {box, (cuuint32_t)p->spec.P};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(&p->tmap, p->spec.esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                            2, base, dims, strides, boxdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    p->tmap_base = nullptr;
-    return DDL_ERR_CUDA;
-  }
-  p->tmap_base = base;
-  p->tmap_stride = stride;
-  p->tmap_box = box;
-  return DDL_OK;
-}
-
 ddl_status_t ddl_allreduce_slab(ddl_plan_t p, void* base, size_t stride, float scale, void* stream) {
   if (!p || !base || p->ov_active) return DDL_ERR_INVALID_ARG;
   const int P = p->spec.P;
@@ -563,40 +522,7 @@ ddl_status_t ddl_allreduce_slab(ddl_plan_t p, void* base, size_t stride, float s
   if (P > 1 && stride < row) return DDL_ERR_INVALID_ARG;
   std::vector<void*> bufs(P);
   for (int r = 0; r < P; ++r) bufs[r] = static_cast<char*>(base) + (size_t)r * stride;
-  bool aligned = false;
-  ddl_status_t st = prepare(p, bufs.data(), &aligned);
-  if (st != DDL_OK) return st;
-  const bool tma = p->kernel == DDL_KERNEL_TMA && aligned && stride % 16 == 0 &&
-                   p->spec.mode != ddl::kStepwise && p->spec.topo != ddl::kTorusND && p->spec.N < (1ull << 31);
-  if (!tma) return ddl_allreduce(p, bufs.data(), scale, stream);
-  const uint32_t box = std::min<uint32_t>(256u, p->spec.tile_bytes / (uint32_t)p->spec.esize);
-  st = encode_slab_map(p, base, stride, box);
-  if (st != DDL_OK) return st;
-  ddl::FoldParams fp;
-  std::memset(&fp, 0, sizeof(fp));
-  fp.items = p->d_items;
-  fp.segs = p->d_segs;
-  fp.orders = p->d_orders;
-  fp.err = p->d_err;
-  fp.item0 = 0;
-  fp.n_segs = (uint32_t)p->tab.segs.size();
-  fp.n_orders = (uint32_t)p->tab.orders.size();
-  fp.P = P;
-  fp.scale = scale;
-  fp.round_hops = (p->spec.esize == 2 && p->spec.mode == ddl::kFused) ? 1 : 0;
-  fp.vector_ok = 1;
-  fp.n_items = (uint32_t)p->tab.items.size();
-  fp.tile_bytes = p->spec.tile_bytes;
-  fp.box_elems = box;
-  fold_shape(p->spec, &fp.inner, &fp.groups);
-  for (int r = 0; r < P; ++r) fp.bufs[r] = bufs[r];
-  nvtxRangePushA("ddl slab (tensor map)");
-  const cudaError_t e =
-      ddl::launch_fold_tma(fp, p->tmap, fp.n_items, p->spec.esize == 2, static_cast<cudaStream_t>(stream));
-  nvtxRangePop();
-  if (e != cudaSuccess) return cuda_status(e);
-  ++p->launches;
-  return DDL_OK;
+  return ddl_allreduce(p, bufs.data(), scale, stream);
 }
 
 ddl_status_t ddl_allreduce_bucket(ddl_plan_t p, int bucket, void* const* bufs, float scale, void* stream) {

@@ -205,7 +205,7 @@ __device__ __forceinline__ bool load_item(const FoldParams& p, char** s_ptr, Ite
 }
 
 // ---------------------------------------------------------------------------
-// Variant 1: register pass.  V columns per thread, B ranks' loads in flight,
+// The register pass.  V columns per thread, B ranks' loads in flight,
 // sized for MINB CTAs per SM.  V * kThreads columns cover the largest item.
 // ---------------------------------------------------------------------------
 #ifndef DDL_LDG_F32_B
@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_nd_h2_kernel(const __grid_co
 }
 
 // ---------------------------------------------------------------------------
-// Variants 2 and 3: shared-memory staged pass with bulk asynchronous copies,
+// The bulk-load pass: shared-memory staged, with bulk asynchronous loads,
 // warp-specialised.
 //
 // Persistent CTAs (one per SM) of 1 producer warp + 8 consumer warps walk
@@ -643,10 +643,9 @@ __global__ void __launch_bounds__(kThreads, 2) fold_nd_h2_kernel(const __grid_co
 // stage's "full" mbarrier with the byte count, and issues one cp.async.bulk
 // per rank (global -> shared).  Consumers wait on "full", fold their columns
 // from shared memory in the schedule's order, and release the stage.  The
-// result goes back either from registers (one 16-byte store per rank, variant
-// 3) or as one shared tile that an elected consumer writes to every rank with
-// cp.async.bulk (shared -> global, variant 2).  The producer never joins a
-// consumer barrier, so its table reads stay off the consumers' path.  Every
+// result goes back from registers, one 16-byte store per rank.  The producer
+// never joins a consumer barrier, so its table reads stay off the consumers'
+// path.  Every
 // wait is bounded: a wait that runs out sets kErrWaitTimeout and the warp
 // leaves its loop; the CTA then drains its own copies (bounded) and returns.
 // ---------------------------------------------------------------------------
@@ -732,38 +731,9 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint3
       : "memory");
 }
 
-__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src_smem)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-// barrier 1 among the consumer warps only (the producer never joins it)
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-}
-// the same barrier, returning whether any consumer passed `flag` (so a
-// timeout is seen by all consumers at once and they leave together)
-__device__ __forceinline__ bool consumer_sync_or(bool flag) {
-  uint32_t any;
-  asm volatile(
-      "{\n\t.reg .pred f, a;\n\t"
-      "setp.ne.u32 f, %1, 0;\n\t"
-      "bar.red.or.pred a, 1, %2, f;\n\t"
-      "selp.u32 %0, 1, 0, a;\n\t}"
-      : "=r"(any)
-      : "r"((uint32_t)flag), "n"(kConsumers)
-      : "memory");
-  return any != 0;
-}
-
-// shared memory: stages x P x tile | 2 x tile output | stages x kMaxP order | meta | barriers
+// shared memory: stages x P x tile | stages x kMaxP order | meta | barriers
 __host__ __device__ constexpr uint32_t bulk_smem_bytes(uint32_t P, uint32_t tile) {
-  return (uint32_t)kStages * P * tile + 2u * tile + (uint32_t)kStages * kMaxP +
+  return (uint32_t)kStages * P * tile + (uint32_t)kStages * kMaxP +
          (uint32_t)(kStages * sizeof(BulkMeta)) + (uint32_t)(2 * kStages * sizeof(uint64_t)) + 16u;
 }
 
@@ -785,14 +755,13 @@ __device__ void fold_scalar_ordered(const FoldParams& p, const uint8_t* order, u
   for (int t = 0; t < p.P; ++t) store_elem<F16>(static_cast<char*>(p.bufs[order[t]]), e, r);
 }
 
-template <bool F16, bool kBulkStore>
+template <bool F16>
 __global__ void __launch_bounds__(kBulkThreads, 1) fold_bulk_kernel(const __grid_constant__ FoldParams p) {
   constexpr int L = F16 ? 8 : 4;
   extern __shared__ __align__(128) unsigned char smem[];
   const uint32_t P = (uint32_t)p.P, T = p.tile_bytes;
   unsigned char* stage = smem;
-  unsigned char* outb = smem + (uint32_t)kStages * P * T;
-  uint8_t* s_order = outb + 2u * T;
+  uint8_t* s_order = smem + (uint32_t)kStages * P * T;
   BulkMeta* s_meta = reinterpret_cast<BulkMeta*>(s_order + kStages * kMaxP);
   uint64_t* full = reinterpret_cast<uint64_t*>(s_meta + kStages);
   uint64_t* empty = full + kStages;
@@ -857,15 +826,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) fold_bulk_kernel(const __grid
   } else {
     // ---------------- consumer warps ----------------
     for (uint32_t s = 0; s < my_n; ++s) {
-      const uint32_t k = s % kStages, j = s & 1u;
-      const bool ok = mbar_wait(&full[k], (s / kStages) & 1u);
-      if constexpr (kBulkStore) {
-        if (tid == 0) bulk_wait_read_1();  // output tile j was read by item s-2's stores
-        if (consumer_sync_or(!ok)) {       // uniform: the named barrier below needs every consumer
-          timed_out = true;
-          break;
-        }
-      } else if (!ok) {
+      const uint32_t k = s % kStages;
+      if (!mbar_wait(&full[k], (s / kStages) & 1u)) {
         timed_out = true;
         break;
       }
@@ -900,11 +862,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) fold_bulk_kernel(const __grid
 #pragma unroll
           for (int l = 0; l < L; ++l) r[l] = __fmul_rn(out[l], p.scale);
           const uint4 res = pack<F16>(r);
-          if constexpr (kBulkStore) {
-            *reinterpret_cast<uint4*>(outb + (size_t)j * T + c * 16u) = res;
-          } else {
-            for (uint32_t t = 0; t < P; ++t) __stcs(reinterpret_cast<uint4*>(p.bufs[t]) + m.vb + c, res);
-          }
+          for (uint32_t t = 0; t < P; ++t) __stcs(reinterpret_cast<uint4*>(p.bufs[t]) + m.vb + c, res);
         }
         // elements of a column cut by the item's ends: straight from global
         const uint64_t nh = (m.ve > m.vb) ? m.vb * L - m.eb : m.ee - m.eb;
@@ -916,16 +874,6 @@ __global__ void __launch_bounds__(kBulkThreads, 1) fold_bulk_kernel(const __grid
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[k]);  // this warp is done with stage k
-      if constexpr (kBulkStore) {
-        fence_async_smem();
-        consumer_sync();
-        if (tid == 0) {
-          if (m.ok && ncols)
-            for (uint32_t r = 0; r < P; ++r)
-              bulk_store(static_cast<char*>(p.bufs[r]) + m.vb * 16u, outb + (size_t)j * T, ncols * 16u);
-          bulk_commit();  // one group per item, so "all but the newest" means item s-1
-        }
-      }
       consumed = s + 1;
     }
     if (timed_out && lane == 0) atomicOr(p.err, kErrWaitTimeout);
@@ -937,22 +885,20 @@ __global__ void __launch_bounds__(kBulkThreads, 1) fold_bulk_kernel(const __grid
   if (warp == kConsumerWarps && lane == 0) s_issued = issued;
   if (tid == 0) s_consumed = consumed;
   __syncthreads();
-  if (tid == 0) {
+  if (tid == 0)
     for (uint32_t q = s_consumed; q < s_issued; ++q) mbar_wait(&full[q % kStages], (q / kStages) & 1u);
-    bulk_wait_all();
-  }
 }
 
 // ---------------------------------------------------------------------------
-// Variant 5: staged through shared memory in rank chunks.  The staged
-// variants above hold all P ranks of a tile in one stage, so at large P a
+// The rank-chunked pass: staged through shared memory in rank chunks.  The
+// bulk-load pass above holds all P ranks of a tile in one stage, so at large P a
 // stage carries little per rank and few consumers have work.  Here a stage
 // holds kChunk ranks (in fold order) of a whole register-pass tile (up to
 // 8 KB per rank): the producer warp streams an item's ranks through the
 // stage ring chunk by chunk with one cp.async.bulk per rank, and each of
 // the 256 consumer threads keeps its two 16-byte columns' fold in registers
 // across the item's chunks, then scales and stores the result to every rank
-// from registers.  Every wait is bounded as in the variants above.  Two
+// from registers.  Every wait is bounded as in the bulk-load pass.  Two
 // ranks per stage, three stages and two CTAs per SM measured fastest (8 ranks
 // per stage and one CTA: 0.92 of the copy peak at P = 16; deeper rings were
 // slower too).
@@ -1136,179 +1082,7 @@ __global__ void __launch_bounds__(kBulkThreads, DDL_CHUNK_MINB) fold_chunked_ker
     for (uint32_t q = s_consumed; q < s_issued; ++q) mbar_wait(&full[q % kCStages], (q / kCStages) & 1u);
 }
 
-// ---------------------------------------------------------------------------
-// Variant 4: staged through shared memory by 2D tensor-map copies.  When the
-// P rank buffers are equally spaced (one slab, rank r at base + r * stride), a
-// tensor map of [P rows x N elements] lets one cp.async.bulk.tensor.2d fetch
-// a box of every rank's next `box_elems` elements at once: P times fewer copy
-// requests than one 1D bulk copy per rank.  Otherwise as variant 3: one
-// producer warp, 8 consumer warps, a 3-stage mbarrier ring, bounded waits,
-// results stored from registers.  Box x coordinates are multiples of 16 bytes
-// (item columns start 16-byte aligned); boxes running past the tensor's end
-// read zeros, and bytes beyond the item are loaded but never used.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void tensor_load_2d(void* dst_smem, const CUtensorMap* map, int32_t x, int32_t y,
-                                               uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-          "r"(smem_addr(dst_smem)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
-}
-
 template <bool F16>
-__global__ void __launch_bounds__(kBulkThreads, 1)
-    fold_tma_kernel(const __grid_constant__ FoldParams p, const __grid_constant__ CUtensorMap tmap) {
-  constexpr int L = F16 ? 8 : 4;
-  extern __shared__ __align__(128) unsigned char smem[];
-  const uint32_t P = (uint32_t)p.P, T = p.tile_bytes;
-  const uint32_t BW = p.box_elems * (F16 ? 2u : 4u);  // bytes of one rank's row in a box
-  unsigned char* stage = smem;
-  uint8_t* s_order = stage + (uint32_t)kStages * P * T + 2u * T;
-  BulkMeta* s_meta = reinterpret_cast<BulkMeta*>(s_order + kStages * kMaxP);
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_meta + kStages);
-  uint64_t* empty = full + kStages;
-
-  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
-  const uint32_t my_n = p.n_items > blockIdx.x ? (p.n_items - 1u - blockIdx.x) / gridDim.x + 1u : 0u;
-  const bool rh = F16 && p.round_hops;
-
-  if (tid == 0) {
-    for (int k = 0; k < kStages; ++k) {
-      mbar_init(&full[k], 1);
-      mbar_init(&empty[k], kConsumerWarps);
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
-  }
-  __syncthreads();
-
-  uint32_t issued = 0, consumed = 0;
-  bool timed_out = false;
-
-  if (warp == kConsumerWarps) {
-    for (uint32_t s = 0; s < my_n; ++s) {
-      const uint32_t k = s % kStages;
-      if (s >= (uint32_t)kStages && !mbar_wait(&empty[k], ((s / kStages) - 1u) & 1u)) {
-        timed_out = true;
-        break;
-      }
-      if (lane == 0) {
-        const Item item = p.items[p.item0 + blockIdx.x + s * gridDim.x];
-        BulkMeta m;
-        m.eb = item.begin;
-        m.ee = item.begin + item.len;
-        m.vb = (m.eb + L - 1) / L;
-        m.ve = m.ee / L;
-        if (m.ve < m.vb) m.ve = m.vb;
-        m.order_off = item.seg * P;
-        m.ok = item.seg < p.n_segs && (uint64_t)item.seg * P + P <= p.n_orders && (m.ve - m.vb) * 16u <= T;
-        m.inner = (uint32_t)p.inner;
-        m.groups = (uint32_t)p.groups;
-        if (!m.ok) atomicOr(p.err, kErrBadItem);
-        s_meta[k] = m;
-      }
-      __syncwarp();
-      const BulkMeta m = s_meta[k];
-      if (m.ok)
-        for (uint32_t t = lane; t < P; t += 32) {
-          const uint32_t r = p.orders[m.order_off + t];
-          s_order[k * kMaxP + t] = (uint8_t)(r < P ? r : 0);
-        }
-      const uint32_t bytes = m.ok ? (uint32_t)(m.ve - m.vb) * 16u : 0u;
-      const uint32_t nbox = (bytes + BW - 1) / BW;
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&full[k], nbox * P * BW);  // release: meta and order published
-      __syncwarp();
-      for (uint32_t j = lane; j < nbox; j += 32)
-        tensor_load_2d(stage + (size_t)k * P * T + (size_t)j * P * BW, &tmap,
-                       (int32_t)(m.vb * L + (uint64_t)j * p.box_elems), 0, &full[k]);
-      issued = s + 1;
-    }
-    if (timed_out && lane == 0) atomicOr(p.err, kErrWaitTimeout);
-  } else {
-    for (uint32_t s = 0; s < my_n; ++s) {
-      const uint32_t k = s % kStages;
-      if (!mbar_wait(&full[k], (s / kStages) & 1u)) {
-        timed_out = true;
-        break;
-      }
-      const BulkMeta m = s_meta[k];
-      const uint8_t* ord = s_order + k * kMaxP;
-      const uint32_t ncols = (uint32_t)(m.ve - m.vb);
-      if (m.ok) {
-        const unsigned char* st = stage + (size_t)k * P * T;
-        for (uint32_t c = tid; c < ncols; c += kConsumers) {
-          const uint32_t o = c * 16u, box = o / BW, within = o % BW;
-          const unsigned char* col = st + (size_t)box * P * BW + within;
-          float in[L], out[L];
-          int h = 0, g = 0;
-          for (uint32_t t0 = 0; t0 < P; t0 += 8) {
-            uint4 raw[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              if (t0 + q < P) raw[q] = *reinterpret_cast<const uint4*>(col + (size_t)ord[t0 + q] * BW);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              if (t0 + q < P) {
-                float f[L];
-                unpack<F16>(raw[q], f);
-                const Ctl ctl = ctl_at((int)(t0 + q), h, g, (int)m.inner, (int)m.groups, (int)P, rh);
-                fold_lanes<L>(in, out, f, ctl);
-                if (++h == (int)m.inner) {
-                  h = 0;
-                  ++g;
-                }
-              }
-            }
-          }
-          float r[L];
-#pragma unroll
-          for (int l = 0; l < L; ++l) r[l] = __fmul_rn(out[l], p.scale);
-          const uint4 res = pack<F16>(r);
-          for (uint32_t t = 0; t < P; ++t) __stcs(reinterpret_cast<uint4*>(p.bufs[t]) + m.vb + c, res);
-        }
-        const uint64_t nh = (m.ve > m.vb) ? m.vb * L - m.eb : m.ee - m.eb;
-        const uint64_t nt = (m.ve > m.vb) ? m.ee - m.ve * L : 0;
-        if (tid < nh + nt) {
-          const uint64_t e = tid < nh ? m.eb + tid : m.ve * L + (tid - nh);
-          fold_scalar_ordered<F16>(p, ord, e, (int)m.inner, (int)m.groups, rh);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[k]);
-      consumed = s + 1;
-    }
-    if (timed_out && lane == 0) atomicOr(p.err, kErrWaitTimeout);
-  }
-  __shared__ uint32_t s_issued, s_consumed;
-  if (warp == kConsumerWarps && lane == 0) s_issued = issued;
-  if (tid == 0) s_consumed = consumed;
-  __syncthreads();
-  if (tid == 0)
-    for (uint32_t q = s_consumed; q < s_issued; ++q) mbar_wait(&full[q % kStages], (q / kStages) & 1u);
-}
-
-template <bool F16>
-cudaError_t launch_tma(const FoldParams& p, const CUtensorMap& tmap, uint32_t n_items, cudaStream_t stream) {
-  const uint32_t smem = bulk_smem_bytes((uint32_t)p.P, p.tile_bytes);
-  int dev = 0, sms = 0, max_smem = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (e != cudaSuccess) return e;
-  const uint32_t es = F16 ? 2u : 4u;
-  if (smem > (uint32_t)max_smem || p.box_elems == 0 || p.box_elems > 256 || (p.box_elems * es) % 16 != 0 ||
-      p.tile_bytes % (p.box_elems * es) != 0)
-    return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(fold_tma_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const uint32_t grid = n_items < (uint32_t)sms ? n_items : (uint32_t)sms;
-  fold_tma_kernel<F16><<<grid, kBulkThreads, smem, stream>>>(p, tmap);
-  return cudaGetLastError();
-}
-
-template <bool F16, bool kBulkStore>
 cudaError_t launch_bulk(const FoldParams& p, uint32_t n_items, cudaStream_t stream) {
   const uint32_t smem = bulk_smem_bytes((uint32_t)p.P, p.tile_bytes);
   int dev = 0, sms = 0, max_smem = 0;
@@ -1317,11 +1091,10 @@ cudaError_t launch_bulk(const FoldParams& p, uint32_t n_items, cudaStream_t stre
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   if (smem > (uint32_t)max_smem || p.tile_bytes % 16 != 0 || p.tile_bytes == 0) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(fold_bulk_kernel<F16, kBulkStore>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
+  e = cudaFuncSetAttribute(fold_bulk_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const uint32_t grid = n_items < (uint32_t)sms ? n_items : (uint32_t)sms;
-  fold_bulk_kernel<F16, kBulkStore><<<grid, kBulkThreads, smem, stream>>>(p);
+  fold_bulk_kernel<F16><<<grid, kBulkThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1378,12 +1151,6 @@ cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t strea
 
 }  // namespace
 
-cudaError_t launch_fold_tma(const FoldParams& p, const CUtensorMap& tmap, uint32_t n_items, bool f16,
-                            cudaStream_t stream) {
-  if (n_items == 0) return cudaSuccess;
-  return f16 ? launch_tma<true>(p, tmap, n_items, stream) : launch_tma<false>(p, tmap, n_items, stream);
-}
-
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream) {
   wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
   return cudaGetLastError();
@@ -1404,10 +1171,7 @@ cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int var
     if (f16) return launch_items(fold_nd_kernel<true, 1, 8>, p, n_items, stream, early_launch);
     return launch_items(fold_nd_kernel<false, 2, 8>, p, n_items, stream, early_launch);
   }
-  if (variant == kVarBulk)
-    return f16 ? launch_bulk<true, true>(p, n_items, stream) : launch_bulk<false, true>(p, n_items, stream);
-  if (variant == kVarBulkLoad)
-    return f16 ? launch_bulk<true, false>(p, n_items, stream) : launch_bulk<false, false>(p, n_items, stream);
+  if (variant == kVarBulkLoad) return f16 ? launch_bulk<true>(p, n_items, stream) : launch_bulk<false>(p, n_items, stream);
   if (variant == kVarChunked)
     return f16 ? launch_chunked<true>(p, n_items, stream) : launch_chunked<false>(p, n_items, stream);
   return f16 ? launch_ldg<true>(p, n_items, stream, early_launch) : launch_ldg<false>(p, n_items, stream, early_launch);

@@ -1,7 +1,6 @@
 // kernels.h -- launch records of the all-reduce kernels (internal).
 #pragma once
 
-#include <cuda.h>  // CUtensorMap (a type only; the encoder is fetched at run time)
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -40,7 +39,6 @@ struct FoldParams {
   int32_t top;         // highest level of size > 1 (its last add is the final one)
   int32_t inner;       // two-level fold: group length (P for ring / multi-ring, X for the torus)
   int32_t groups;      // number of groups (1, or Y for the torus)
-  uint32_t box_elems;  // tensor-map pass: box width in elements (box height = P)
   void* bufs[kMaxP];   // rank r's buffer
 };
 
@@ -78,13 +76,9 @@ struct StepParams {
   void* bufs[kMaxP];
 };
 
-// Variants of the fused pass.
-enum FoldVariant : int { kVarLdg = 1, kVarBulk = 2, kVarBulkLoad = 3, kVarChunked = 4 };
-
-// The staged pass whose loads are 2D tensor-map copies of [P ranks x box]
-// from equally spaced rank buffers (ddl_allreduce_slab).
-cudaError_t launch_fold_tma(const FoldParams& p, const CUtensorMap& tmap, uint32_t n_items, bool f16,
-                            cudaStream_t stream);
+// Variants of the fused pass: the register pass, the bulk-load staged pass
+// (all ranks of a tile per stage), the rank-chunked staged pass.
+enum FoldVariant : int { kVarLdg = 1, kVarBulkLoad = 3, kVarChunked = 4 };
 
 // early_launch: launch the register passes as programmatic dependents of the
 // kernel before them on the stream (they read only the plan's tables before

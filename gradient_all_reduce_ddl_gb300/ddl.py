@@ -31,7 +31,7 @@ DDL_RING, DDL_MULTIRING, DDL_TORUS = 0, 1, 2
 # ddl_mode_t
 DDL_MODE_FUSED, DDL_MODE_STEPWISE, DDL_MODE_RANKORDER = 0, 1, 2
 # ddl_kernel_t
-DDL_KERNEL_AUTO, DDL_KERNEL_LDG, DDL_KERNEL_BULK, DDL_KERNEL_BULK_LOAD, DDL_KERNEL_TMA, DDL_KERNEL_CHUNKED = 0, 1, 2, 3, 4, 5
+DDL_KERNEL_AUTO, DDL_KERNEL_LDG, DDL_KERNEL_BULK_LOAD, DDL_KERNEL_CHUNKED = 0, 1, 3, 5
 
 EXPORTS = [
     "ddl_plan_create", "ddl_plan_set_layers", "ddl_plan_set_mode", "ddl_plan_set_kernel", "ddl_allreduce",
@@ -266,8 +266,8 @@ def ddl_noalloc_check(stream=None):
 TOPOLOGIES = {"ring": DDL_RING, "multiring": DDL_MULTIRING, "torus": DDL_TORUS, "torus_nd": DDL_RING}
 DTYPES = {"f32": DDL_FP32, "f16": DDL_FP16}
 MODES = {"fused": DDL_MODE_FUSED, "stepwise": DDL_MODE_STEPWISE, "rankorder": DDL_MODE_RANKORDER}
-KERNELS = {"auto": DDL_KERNEL_AUTO, "ldg": DDL_KERNEL_LDG, "bulk": DDL_KERNEL_BULK, "bulkload": DDL_KERNEL_BULK_LOAD,
-           "tma": DDL_KERNEL_TMA, "chunked": DDL_KERNEL_CHUNKED}
+KERNELS = {"auto": DDL_KERNEL_AUTO, "ldg": DDL_KERNEL_LDG, "bulkload": DDL_KERNEL_BULK_LOAD,
+           "chunked": DDL_KERNEL_CHUNKED}
 
 
 class Plan:

@@ -90,16 +90,16 @@ typedef enum {
 typedef enum {
   DDL_KERNEL_AUTO = 0,  /* the library's choice */
   DDL_KERNEL_LDG = 1,   /* fused pass with 16-byte register loads and stores */
-  DDL_KERNEL_BULK = 2,  /* fused pass staged through shared memory by bulk async copies,
-                           loads and stores */
-  DDL_KERNEL_BULK_LOAD = 3, /* bulk async loads into shared memory, stores from registers */
-  DDL_KERNEL_TMA = 4,       /* ddl_allreduce_slab only: 2D tensor-map loads of every rank's
-                               next tile in one copy, stores from registers (elsewhere and
-                               when the slab does not qualify: the register pass) */
+  /* 2 is not used (a staged pass with bulk stores, removed: it was slower
+     than the register pass at every P measured) */
+  DDL_KERNEL_BULK_LOAD = 3, /* bulk async loads of all ranks' tiles into shared memory, stores
+                               from registers (the zero-copy host pass's kernel) */
+  /* 4 is not used (2D tensor-map loads from a slab, removed: slower than
+     the register pass at every P measured) */
   DDL_KERNEL_CHUNKED = 5    /* bulk async loads of the register pass's tiles (up to 8 KB per
                                rank) into shared memory, 2 ranks per stage in fold order,
                                the fold kept in registers across an item's stages, stores
-                               from registers */
+                               from registers (the overlap side stream's kernel) */
 } ddl_kernel_t;
 
 typedef struct ddl_plan* ddl_plan_t;
@@ -160,8 +160,9 @@ ddl_status_t ddl_plan_set_torus_dims(ddl_plan_t plan, int ndims, const int* dims
  * sum element by element.  Host-only. */
 ddl_status_t ddl_plan_set_mode(ddl_plan_t plan, ddl_mode_t mode);
 
-/* Selects the fused kernel variant (default DDL_KERNEL_AUTO).  Results are
- * identical for every variant.  Host-only. */
+/* Selects the fused kernel variant (default DDL_KERNEL_AUTO; values 2 and 4
+ * return DDL_ERR_INVALID_ARG).  Results are identical for every variant.
+ * Host-only. */
 ddl_status_t ddl_plan_set_kernel(ddl_plan_t plan, ddl_kernel_t kernel);
 
 /* All-reduces every bucket, in place, in issue order (fused and rank-order
@@ -206,14 +207,8 @@ ddl_status_t ddl_allreduce_sgd(ddl_plan_t plan, void* const* grad_bufs, float* c
 
 /* ddl_allreduce for rank buffers laid out in one slab: rank r's N elements
  * start at base + r * rank_stride_bytes (rank_stride_bytes >= N * element
- * size; the slab is caller-owned device memory).  Results equal
- * ddl_allreduce's on the same buffers.  With DDL_KERNEL_TMA, a 2D tensor map
- * over the slab (P rows, stride rank_stride_bytes) lets one
- * cp.async.bulk.tensor copy bring a tile of every rank into shared memory.
- * That path needs a 16-byte aligned base and stride, N < 2^31, a fused or
- * rank-order plan of a ring, multi-ring or 2D torus, and P <= 256; otherwise
- * the call runs the register pass.  The tensor map is encoded on the first
- * call for a given slab and kept by the plan. */
+ * size when P > 1; the slab is caller-owned device memory).  The same call,
+ * with the P pointers computed from the slab. */
 ddl_status_t ddl_allreduce_slab(ddl_plan_t plan, void* base, size_t rank_stride_bytes, float scale, void* stream);
 
 /* All-reduces bucket b only (0 <= b < ddl_plan_num_buckets). */

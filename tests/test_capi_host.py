@@ -117,7 +117,7 @@ def test_workload_tables_match_oracle(ddl, name):
 
 
 @pytest.mark.parametrize("case", [CASES[2], CASES[5], CASES[7], CASES[9]])
-@pytest.mark.parametrize("kernel", ["bulk", "chunked"])
+@pytest.mark.parametrize("kernel", ["bulkload", "chunked"])
 def test_staged_kernel_tables_match_oracle(ddl, case, kernel):
     """Selecting a staged kernel rebuilds the work items at its tile size (the
     rank-chunked pass keeps the register pass's); the fold orders stay the
@@ -199,13 +199,14 @@ def test_invalid_arguments(ddl):
 
 
 def test_kernel_choice_range(ddl):
-    """Every ddl_kernel_t value is accepted on a host-only plan; the next one
-    is refused."""
+    """Every ddl_kernel_t value is accepted on a host-only plan; the unused
+    values 2 and 4 (passes removed from the library), the next one and a
+    negative one are refused."""
     with ddl.Plan(8, 10_000) as plan:
-        for k in range(0, 6):
+        for k in (0, 1, 3, 5):
             assert ddl._lib.ddl_plan_set_kernel(plan.handle, k) == ddl.DDL_OK, k
-        assert ddl._lib.ddl_plan_set_kernel(plan.handle, 6) == ddl.DDL_ERR_INVALID_ARG
-        assert ddl._lib.ddl_plan_set_kernel(plan.handle, -1) == ddl.DDL_ERR_INVALID_ARG
+        for k in (2, 4, 6, -1):
+            assert ddl._lib.ddl_plan_set_kernel(plan.handle, k) == ddl.DDL_ERR_INVALID_ARG, k
 
 
 def test_layer_sizes_that_would_wrap_are_refused(ddl):
@@ -237,3 +238,4 @@ def test_noalloc_refuses_oversized_problems_before_any_gpu_work(ddl):
     with pytest.raises(ddl.DDLError) as ei:
         ddl.ddl_allreduce_noalloc(2, 100, ddl.DDL_FP32, torus, 0, None, fake, 0.5)
     assert ei.value.status == ddl.DDL_ERR_INVALID_ARG
+

@@ -96,7 +96,7 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("kernel", ["ldg", "bulk", "bulkload", "chunked"])
+@pytest.mark.parametrize("kernel", ["ldg", "bulkload", "chunked"])
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
 def test_fused_matches_oracle(ddl, case, dtype, kernel):
@@ -105,7 +105,7 @@ def test_fused_matches_oracle(ddl, case, dtype, kernel):
     _check_exact(ddl, _w(dtype=dtype, **case), kernel=kernel)
 
 
-@pytest.mark.parametrize("kernel", ["ldg", "bulk", "chunked"])
+@pytest.mark.parametrize("kernel", ["ldg", "bulkload", "chunked"])
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
 @pytest.mark.parametrize("case", [SMALL[4], SMALL[7], SMALL[11], SMALL[16], SMALL[18]])
 def test_fused_unaligned_buffers_match_oracle(ddl, case, dtype, kernel):
@@ -186,13 +186,13 @@ def test_allreduce_sgd_matches_oracle(ddl, case, mom, keep):
         assert np.array_equal(to_numpy_bits(grads[r]), g_ref[r] if keep else host[r]), ("grads", r)
 
 
-@pytest.mark.parametrize("kernel", ["bulk", "bulkload", "tma", "chunked"])
+@pytest.mark.parametrize("kernel", ["bulkload", "chunked"])
 @pytest.mark.parametrize("P", [2, 4])
 def test_small_p_with_a_staged_kernel_choice(ddl, kernel, P):
     """P <= 4 with a staged kernel chosen.  A staged tile once grew to 16 KB
-    per rank at such P, more than the register pass covers, and the register
-    pass runs those items for ddl_allreduce with the tensor-map choice and
-    for the fused SGD pass with any choice: both must match the oracle."""
+    per rank at such P, more than the register pass covers, and the fused
+    SGD pass runs the plan's items in the register pass's shape whatever the
+    choice: the all-reduce and the SGD pass must match the oracle."""
     w = _w(P=P, N=200_003, seed=77)
     _check_exact(ddl, w, kernel=kernel)
     host = _host_inputs(w)
@@ -311,17 +311,17 @@ SLAB_CASES = [
 ]
 
 
-@pytest.mark.parametrize("kernel", ["tma", "ldg", "bulkload"])
+@pytest.mark.parametrize("kernel", ["ldg", "bulkload"])
 @pytest.mark.parametrize("case", SLAB_CASES, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
 def test_slab_matches_oracle(ddl, case, kernel):
-    """Rank buffers in one slab (rank r at base + r * stride): the 2D
-    tensor-map pass and the other kernels give the oracle's bits."""
+    """Rank buffers in one slab (rank r at base + r * stride) give the
+    oracle's bits, aligned or not."""
     w = _w(seed=71, **case)
     host = _host_inputs(w)
     ref = [h.copy() for h in host]
     oracle.emulate(oracle_cfg(w), ref, w.scale)
     es = w.esize
-    for pad in (0, 24):                           # pad 24 B: stride not a multiple of 16 -> register pass
+    for pad in (0, 24):                           # pad 24 B: stride not a multiple of 16 -> element-wise path
         stride = (w.N * es + 255) // 256 * 256 + pad
         slab = torch.zeros(stride * w.P // 2 + 16, dtype=torch.int16, device=DEV)
         base = slab.data_ptr()
@@ -528,7 +528,7 @@ FULL = ["ring4_int", "torus4x4_resnet50", "torus8x4_resnet50_f16", "multiring64_
         "multiring16_lm300m", "torus4x4_lm300m", "torus4x4x4_resnet101", "torus4x4x2_resnet50_f16"]
 
 
-@pytest.mark.parametrize("kernel", ["auto", "bulk", "bulkload", "chunked"])
+@pytest.mark.parametrize("kernel", ["auto", "bulkload", "chunked"])
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_workload_sampled(ddl, name, kernel):
     w = synth.WORKLOADS[name]
@@ -941,7 +941,7 @@ def test_bounded_wait_timeout_is_reported_and_context_survives(ddl):
     host = _host_inputs(w)
     ref = [h.copy() for h in host]
     oracle.emulate(oracle_cfg(w), ref, w.scale)
-    with ddl.Plan.for_workload(w, kernel="bulk") as plan:
+    with ddl.Plan.for_workload(w, kernel="bulkload") as plan:
         assert ddl.ddl_plan_check(plan.handle) == ddl.DDL_OK
         ddl.ddl_selftest_wait_timeout(plan.handle, 50_000)
         assert ddl.ddl_plan_check(plan.handle) == ddl.DDL_ERR_DEVICE_CHECK
