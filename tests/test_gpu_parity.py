@@ -624,6 +624,41 @@ def test_overlap_end_reduces_buckets_never_signalled(ddl, signalled):
         assert np.array_equal(to_numpy_bits(bufs[r]), ref[r]), r
 
 
+@pytest.mark.parametrize("mode", ["fused", "rankorder", "stepwise"])
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("topo", [dict(topo="multiring", k=3), dict(topo="torus", X=4, Y=2)])
+def test_overlap_equals_allreduce_in_every_mode(ddl, mode, dtype, topo):
+    """The bucket scheduler (side-stream launches, the rank-chunked pass where
+    the plan's kernel choice allows) gives, in every mode and dtype, the bits
+    the same plan's ddl_allreduce gives."""
+    es = 2 if dtype == "f16" else 4
+    w = _w(P=8, N=300_007, dtype=dtype, layers=[60_000, 90_007, 50_000, 100_000], bucket_bytes=60_000 * es,
+           seed=13, **topo)
+    host = _host_inputs(w)
+    a = device_bufs_from_host(host, DEV)
+    b = device_bufs_from_host(host, DEV)
+    torch.cuda.synchronize()
+    main = torch.cuda.Stream()
+    with ddl.Plan.for_workload(w, mode=mode) as plan:
+        assert plan.num_buckets >= 3
+        plan.allreduce(a, w.scale)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(main):
+            plan.overlap_begin(b, w.scale, stream=main)
+            for q in range(plan.num_buckets):
+                plan.bucket_ready(q, stream=main)
+            plan.overlap_end(stream=main)
+        main.synchronize()
+        torch.cuda.synchronize()
+        plan.check()
+    for r in range(w.P):
+        assert np.array_equal(to_numpy_bits(b[r]), to_numpy_bits(a[r])), r
+    if mode != "rankorder":
+        ref = [h.copy() for h in host]
+        oracle.emulate(oracle_cfg(w), ref, w.scale)
+        assert np.array_equal(to_numpy_bits(b[0]), ref[0])
+
+
 @pytest.mark.parametrize("name", ["multiring64_resnet101", "torus4x4x4_resnet101"])
 def test_full_size_overlap_sampled(ddl, name):
     """The bucket scheduler at full size: the 7 ResNet-101 buckets written
