@@ -574,7 +574,9 @@ def e2e_leg(plans, wls, bufs, stream, dev, ws: int, e2e_steps: int) -> dict:
 def secondary_leg(ddl, name: str, dev, stream, peak: float, samples: dict, target_ms: float = 250.0) -> dict:
     """One of the other problems, timed on its own after the headline: one
     all-reduce of fresh inputs (its result sampled for the oracle leg), three
-    warm-up calls, then enough calls for about `target_ms` of device time."""
+    warm-up calls, then enough calls for about `target_ms` of device time.
+    A bucketed problem also times its bucket scheduler against a synthetic
+    backward (overlap_study)."""
     import torch
     w = synth.WORKLOADS[name]
     bufs, _, _ = alloc_bufs(w, dev, stream)
@@ -619,6 +621,10 @@ def secondary_leg(ddl, name: str, dev, stream, peak: float, samples: dict, targe
                 out["us_per_call"] = round(ms * 1e3, 3)
                 out["us_per_allreduce_graph_replay"] = round(g_total * 1e3 / (reps * per_graph), 3)
                 del graph
+            if plan.num_buckets > 1:
+                # the bucket scheduler against the same step run sequentially
+                out["overlap"] = overlap_study(plan, bufs, w, stream, steps=10)
+                out["overlap"]["allreduce_alone_ms"] = round(ms, 4)
             torch.cuda.synchronize(dev)
     finally:
         plan.close()
