@@ -9,6 +9,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -90,9 +91,18 @@ void drop_zero_copy(ddl_plan* p) {
   delete z;
 }
 
+// Host-side fault injection for the failure tests: with the environment
+// variable DDL_INJECT_ALLOC_FAILURE=1, uploading a plan's tables fails as if
+// the device were out of memory (no GPU call is made for it).
+bool alloc_failure_injected() {
+  const char* v = std::getenv("DDL_INJECT_ALLOC_FAILURE");
+  return v && v[0] == '1' && v[1] == '\0';
+}
+
 template <typename T>
 cudaError_t upload(T** dst, const std::vector<T>& v) {
   if (v.empty()) return cudaSuccess;
+  if (alloc_failure_injected()) return cudaErrorMemoryAllocation;
   cudaError_t e = cudaMalloc(reinterpret_cast<void**>(dst), v.size() * sizeof(T));
   if (e != cudaSuccess) return e;
   return cudaMemcpy(*dst, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice);

@@ -38,6 +38,10 @@
  *  - A plan is not thread-safe: do not call into one plan from two host
  *    threads at once, and do not queue two all-reduces of one plan that may
  *    run concurrently on the GPU over the same buffers.
+ *  - Failure testing: with the environment variable
+ *    DDL_INJECT_ALLOC_FAILURE=1, the upload of a plan's device tables fails
+ *    as if the device were out of memory (DDL_ERR_OOM, nothing queued); the
+ *    plan uploads them at its next call once the variable is unset.
  */
 #ifndef DDL_H_
 #define DDL_H_

@@ -991,6 +991,32 @@ def test_bounded_wait_timeout_is_reported_and_context_survives(ddl):
             ddl.ddl_selftest_wait_timeout(plan.handle, 0)
 
 
+def test_injected_allocation_failure_returns_oom_and_the_plan_recovers(ddl, monkeypatch):
+    """Host-side fault injection: with DDL_INJECT_ALLOC_FAILURE=1 the upload
+    of the plan's device tables fails as if the device were out of memory.
+    The all-reduce returns DDL_ERR_OOM and touches no buffer; once the
+    variable is gone the same plan uploads its tables and is bit-exact."""
+    w = _w(P=5, N=30_011, topo="multiring", k=2, seed=17)
+    host = _host_inputs(w)
+    ref = [h.copy() for h in host]
+    oracle.emulate(oracle_cfg(w), ref, w.scale)
+    bufs = device_bufs_from_host(host, DEV)
+    with ddl.Plan.for_workload(w) as plan:
+        monkeypatch.setenv("DDL_INJECT_ALLOC_FAILURE", "1")
+        with pytest.raises(ddl.DDLError) as ei:
+            plan.allreduce(bufs, w.scale)
+        assert ei.value.status == ddl.DDL_ERR_OOM
+        torch.cuda.synchronize()
+        for r in range(w.P):
+            assert np.array_equal(to_numpy_bits(bufs[r]), host[r]), r   # nothing ran
+        monkeypatch.delenv("DDL_INJECT_ALLOC_FAILURE")
+        plan.allreduce(bufs, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    for r in range(w.P):
+        assert np.array_equal(to_numpy_bits(bufs[r]), ref[r]), r
+
+
 def test_launch_counts_and_checks(ddl):
     w = _w(P=16, N=100_000, topo="torus", X=4, Y=4, bucket_bytes=100_000)
     bufs = device_bufs_generated(w, DEV)
