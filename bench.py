@@ -515,6 +515,27 @@ def kernel_bytes_of(plan, w, mode: str) -> int:
     return w.min_bytes
 
 
+def host_memory_short(need: int, ws: int, avail: int | None = None) -> str | None:
+    """Why the page-locked buffers of the e2e leg do not fit on this host, or
+    None.  Every replica on a host pins its own buffers at once, and the
+    answer is the same on every rank (a rank that skipped the leg would leave
+    the others waiting in its max-over-ranks timing)."""
+    if avail is None:
+        try:
+            with open("/proc/meminfo") as fh:
+                avail = next(int(line.split()[1]) * 1024 for line in fh if line.startswith("MemAvailable:"))
+        except (OSError, StopIteration, ValueError):
+            avail = None
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    short = avail is not None and avail < need * local_ranks + (8 << 30)
+    if reduce_max(1.0 if short else 0.0, ws) == 0:
+        return None
+    if short:
+        return (f"host memory: {avail / 1e9:.1f} GB available, {need * local_ranks / 1e9:.1f} GB of page-locked "
+                f"buffers needed")
+    return "host memory short on another rank"
+
+
 def e2e_leg(plans, wls, bufs, stream, dev, ws: int, e2e_steps: int) -> dict:
     """The same step through ddl_allreduce_host on page-locked host buffers:
     every call moves P*N*e bytes in and P*N*e out over the host link inside
@@ -523,16 +544,9 @@ def e2e_leg(plans, wls, bufs, stream, dev, ws: int, e2e_steps: int) -> dict:
     import torch
     w0 = wls[0]
     tdt = bufs[0].dtype
-    need = w0.P * w0.N * w0.esize
-    try:
-        with open("/proc/meminfo") as fh:
-            avail = next(int(line.split()[1]) * 1024 for line in fh if line.startswith("MemAvailable:"))
-    except (OSError, StopIteration, ValueError):
-        avail = None
-    if avail is not None and avail < need + (8 << 30):
-        return {"value": None, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
-                "skipped": f"host memory: {avail / 1e9:.1f} GB available, {need / 1e9:.1f} GB of page-locked "
-                           f"buffers needed"}
+    why = host_memory_short(w0.P * w0.N * w0.esize, ws)
+    if why:
+        return {"value": None, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0, "skipped": why}
     host = [torch.empty(w0.N, dtype=tdt, pin_memory=True) for _ in range(w0.P)]
     for r in range(w0.P):
         host[r].copy_(bufs[r])
