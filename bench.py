@@ -65,9 +65,9 @@ SECONDARY = ("ring4_int", "torus4x4_resnet50", "torus8x4_resnet50_f16", "multiri
 # algorithmic bytes; a changed kernel source reports null.
 NCU_TRAFFIC = {
     # P = 16 x 20,000,000 fp32 (1.28 GB resident, above L2): 2.56 GB algorithmic per launch
-    ("ring", "f32", "ldg", "8607b38eea7c1249"): (1_280_199_168 + 1_220_699_136, 2_560_000_000),
-    ("multiring", "f32", "ldg", "8607b38eea7c1249"): (1_280_317_952 + 1_219_991_040, 2_560_000_000),
-    ("torus", "f32", "ldg", "8607b38eea7c1249"): (1_280_199_424 + 1_220_781_824, 2_560_000_000),
+    ("ring", "f32", "ldg", "a40275dbbceb0c01"): (1_280_227_584 + 1_220_563_968, 2_560_000_000),
+    ("multiring", "f32", "ldg", "a40275dbbceb0c01"): (1_280_250_368 + 1_220_319_488, 2_560_000_000),
+    ("torus", "f32", "ldg", "a40275dbbceb0c01"): (1_280_199_936 + 1_220_656_896, 2_560_000_000),
 }
 
 KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]
