@@ -387,6 +387,119 @@ __global__ void __launch_bounds__(kThreads) fold_small_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
+// Latency pass: small items of two-level folds (ring, multi-ring, 2D torus;
+// any dtype and rounding) whose P tiles fit in shared memory.  The register
+// pass folds P ranks in batches of 8, one global round trip per batch, which
+// dominates when a buffer is too small to keep the GPU busy.  Here the CTA
+// loads all P ranks' columns of its item into shared memory at once (one
+// round trip, every thread issuing loads), folds each row group of the
+// schedule in parallel (thread per group and column), folds the group totals
+// (thread per column), and stores the result to every rank from shared
+// memory, all threads at once.  The adds, their order and their roundings are
+// exactly those of the register pass: a group is the left fold of its inner
+// ranks, each add rounded to binary16 where a hop would carry it; the group
+// totals are left-folded, every add rounded but the final one.
+// Shared memory: P x tile bytes of data (fold position t at t * tile), then
+// groups x columns binary32 group totals (L lanes each), then one 16-byte
+// result per column.
+// ---------------------------------------------------------------------------
+__host__ __device__ constexpr uint32_t lat_smem_bytes(uint32_t P, uint32_t groups, uint32_t tile, uint32_t lanes) {
+  return P * tile + groups * (tile / 16u) * lanes * 4u + (tile / 16u) * 16u;
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(kThreads) fold_lat_kernel(const __grid_constant__ FoldParams p) {
+  constexpr int L = F16 ? 8 : 4;  // elements per 16-byte column
+  extern __shared__ __align__(16) unsigned char s_lat[];
+  __shared__ char* s_ptr[kMaxP];
+  Item s_item;
+  griddep_launch_dependents();
+  if (!load_item(p, s_ptr, &s_item)) return;
+  griddep_wait();
+
+  const int P = p.P, inner = p.inner, groups = p.groups;
+  const bool rh = F16 && p.round_hops;
+  const uint32_t T = p.tile_bytes;
+  const uint64_t eb = s_item.begin, ee = eb + s_item.len;
+  const uint64_t vb = (eb + L - 1) / L, ve = ee / L;
+  if (!p.vector_ok || vb >= ve) {
+    for (uint64_t e = eb + threadIdx.x; e < ee; e += kThreads)
+      fold_scalar<F16>(s_ptr, e, P, inner, groups, rh, p.scale);
+    return;
+  }
+  const uint32_t ncols = (uint32_t)(ve - vb);  // <= T / 16
+  float* s_tot = reinterpret_cast<float*>(s_lat + (size_t)P * T);
+  uint4* s_res = reinterpret_cast<uint4*>(s_lat + (size_t)P * T + (size_t)groups * (T / 16u) * L * 4u);
+
+  // every fold position's columns, all loads in flight together
+  for (uint32_t i = threadIdx.x; i < (uint32_t)P * ncols; i += kThreads) {
+    const uint32_t t = i / ncols, c = i % ncols;
+    *reinterpret_cast<uint4*>(s_lat + (size_t)t * T + c * 16u) =
+        __ldcs(reinterpret_cast<const uint4*>(s_ptr[t]) + vb + c);
+  }
+  __syncthreads();
+
+  // each row group of each column: the left fold of its inner positions
+  for (uint32_t i = threadIdx.x; i < (uint32_t)groups * ncols; i += kThreads) {
+    const int g = (int)(i / ncols);
+    const uint32_t c = i % ncols;
+    float a[L];
+    for (int h = 0; h < inner; ++h) {
+      const int t = g * inner + h;
+      float f[L];
+      unpack<F16>(*reinterpret_cast<const uint4*>(s_lat + (size_t)t * T + c * 16u), f);
+      if (h == 0) {
+#pragma unroll
+        for (int l = 0; l < L; ++l) a[l] = f[l];
+      } else {
+        // rounded where the sum travels again: every inner add but the final
+        // add of a single-group fold
+        const bool round = rh && !(t == P - 1 && groups == 1);
+#pragma unroll
+        for (int l = 0; l < L; ++l) {
+          const float v = __fadd_rn(a[l], f[l]);
+          a[l] = round ? round_h(v) : v;
+        }
+      }
+    }
+#pragma unroll
+    for (int l = 0; l < L; ++l) s_tot[((size_t)g * (T / 16u) + c) * L + l] = a[l];
+  }
+  __syncthreads();
+
+  // each column: the left fold of its group totals, scaled, in storage form
+  for (uint32_t c = threadIdx.x; c < ncols; c += kThreads) {
+    float o[L];
+#pragma unroll
+    for (int l = 0; l < L; ++l) o[l] = s_tot[(size_t)c * L + l];
+    for (int g = 1; g < groups; ++g) {
+      const bool round = rh && g != groups - 1;  // the last group's add is the final one
+#pragma unroll
+      for (int l = 0; l < L; ++l) {
+        const float v = __fadd_rn(o[l], s_tot[((size_t)g * (T / 16u) + c) * L + l]);
+        o[l] = round ? round_h(v) : v;
+      }
+    }
+#pragma unroll
+    for (int l = 0; l < L; ++l) o[l] = __fmul_rn(o[l], p.scale);
+    s_res[c] = pack<F16>(o);
+  }
+  __syncthreads();
+
+  // the result to every rank, all threads at once
+  for (uint32_t i = threadIdx.x; i < (uint32_t)P * ncols; i += kThreads) {
+    const uint32_t t = i / ncols, c = i % ncols;
+    __stcs(reinterpret_cast<uint4*>(s_ptr[t]) + vb + c, s_res[c]);
+  }
+  // the few elements of a cut column at either end of the item
+  const uint64_t nh = vb * L - eb, nt = ee - ve * L;
+  if (threadIdx.x < nh + nt) {
+    const uint64_t e = threadIdx.x < nh ? eb + threadIdx.x : ve * L + (threadIdx.x - nh);
+    fold_scalar<F16>(s_ptr, e, P, inner, groups, rh, p.scale);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // n-D torus register pass: the fold is d nested left folds (innermost over
 // dim 0 from chunk c_0, then dim 1, ...).  A cascade of one accumulator per
 // level follows the ranks in fold order: a finished group of level l is added
@@ -1182,11 +1295,11 @@ cudaError_t launch_chunked(const FoldParams& p, uint32_t n_items, cudaStream_t s
 
 // One CTA of kThreads per work item, optionally as a programmatic dependent.
 cudaError_t launch_items(void (*kernel)(FoldParams), const FoldParams& p, uint32_t n_items, cudaStream_t stream,
-                         bool early) {
+                         bool early, uint32_t smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_items);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1196,12 +1309,47 @@ cudaError_t launch_items(void (*kernel)(FoldParams), const FoldParams& p, uint32
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// The latency pass takes small items (at most 4 KB per rank) of plans with at
+// least kLatMinP ranks whose shared-memory footprint stays within kLatMaxSmem.
+// Measured per all-reduce in graph replay: at P = 32 (8x4 fp16 torus, 16,384
+// elements per rank) 5.33 us against 7.18 us in the register pass, at P = 64
+// (4-ring multi-ring, fp32) 4.72 against 8.62 us; at P = 16 its three barriers
+// cost more than the register pass's two batches of loads (ring 3.20 against
+// 3.07 us), so smaller plans keep the register or small-item pass.
+#ifndef DDL_LAT_MIN_P
+#define DDL_LAT_MIN_P 32
+#endif
+constexpr int kLatMinP = DDL_LAT_MIN_P;
+constexpr uint32_t kLatMaxSmem = 96u * 1024u;
+
+template <bool F16>
+cudaError_t launch_lat(const FoldParams& p, uint32_t n_items, cudaStream_t stream, bool early, uint32_t smem) {
+  // the opt-in above 48 KB, once per device
+  static int ready[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!ready[dev]) {
+    e = cudaFuncSetAttribute(fold_lat_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLatMaxSmem);
+    if (e != cudaSuccess) return e;
+    ready[dev] = 1;
+  }
+  return launch_items(fold_lat_kernel<F16>, p, n_items, stream, early, smem);
+}
+
 template <bool F16>
 cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t stream, bool early) {
   // two 16-byte columns per thread cover kTileBytes per rank; a larger item
   // is refused (the element-wise path, taken for unaligned buffers, covers
   // any item)
   if (p.vector_ok && p.tile_bytes > (uint32_t)kTileBytes) return cudaErrorInvalidValue;
+  // small items of many ranks: the latency pass
+  if (p.vector_ok && p.tile_bytes <= (uint32_t)kThreads * 16u && p.P >= kLatMinP && p.groups >= 1 &&
+      p.inner >= 1 && (int64_t)p.inner * p.groups == p.P) {
+    const uint32_t smem = lat_smem_bytes((uint32_t)p.P, (uint32_t)p.groups, p.tile_bytes, F16 ? 8u : 4u);
+    if (smem <= kLatMaxSmem) return launch_lat<F16>(p, n_items, stream, early, smem);
+  }
   // small items of a single unrounded group: the small-item pass (one column
   // per thread covers up to kThreads * 16 bytes per rank)
   const bool unrounded = !F16 || !p.round_hops;
