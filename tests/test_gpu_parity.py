@@ -186,6 +186,57 @@ def test_allreduce_sgd_matches_oracle(ddl, case, mom, keep):
         assert np.array_equal(to_numpy_bits(grads[r]), g_ref[r] if keep else host[r]), ("grads", r)
 
 
+# Small buffers (items of 1-4 KB per rank): P >= 32 takes the latency pass
+# (shared-memory staged, row groups folded in parallel) while its tiles fit in
+# 96 KB; smaller single-group unrounded folds take the small-item pass; the
+# rest the register pass.  N is odd, so items end in cut columns.
+SMALL_BUFFERS = [
+    dict(P=32, N=40_001, topo="torus", X=8, Y=4),
+    dict(P=32, N=9_999, topo="torus", X=4, Y=8),
+    dict(P=32, N=20_003, topo="torus", X=1, Y=32),
+    dict(P=32, N=20_003, topo="torus", X=32, Y=1),
+    dict(P=48, N=30_007, topo="multiring", k=3, bucket_bytes=40_000),
+    dict(P=64, N=16_385, topo="multiring", k=4),
+    dict(P=64, N=70_001, topo="torus", X=8, Y=8),
+    dict(P=96, N=20_001, topo="torus", X=12, Y=8),
+    dict(P=40, N=5_001, layers=[1_000, 2_001, 2_000], bucket_bytes=4_000),
+    dict(P=8, N=40_001, topo="multiring", k=2),
+    dict(P=12, N=30_001, topo="torus", X=4, Y=3),
+]
+
+
+@pytest.mark.parametrize("mode", ["fused", "rankorder"])
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("case", SMALL_BUFFERS, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_small_buffer_passes_match_oracle(ddl, case, dtype, mode):
+    w = _w(dtype=dtype, seed=23, **case)
+    if mode == "fused":
+        _check_exact(ddl, w)
+        return
+    host = _host_inputs(w)
+    bufs = device_bufs_from_host(host, DEV)
+    with ddl.Plan.for_workload(w, mode="rankorder") as plan:
+        plan.allreduce(bufs, w.scale)
+        torch.cuda.synchronize()
+        plan.check()
+    got0 = to_numpy_bits(bufs[0])
+    # rank order is one binary32 left fold in rank order: the same bits from
+    # the element-wise path on unaligned copies of the inputs
+    big = []
+    for h in host:
+        t = torch.zeros(w.N + 1, dtype=torch_dtype(w.dtype), device=DEV)
+        t[1:] = device_bufs_from_host([h], DEV)[0]
+        big.append(t[1:])
+    with ddl.Plan.for_workload(w, mode="rankorder") as plan:
+        plan.allreduce(big, w.scale)
+        torch.cuda.synchronize()
+    assert np.array_equal(got0, to_numpy_bits(big[0]))
+    norm, elem = rankorder_margins(host, got0, w.scale, dtype)
+    assert norm <= (1e-6 if dtype == "f32" else 2e-3) and elem <= 1.0, (norm, elem)
+    for r in range(1, w.P):
+        assert np.array_equal(to_numpy_bits(bufs[r]), got0), r
+
+
 @pytest.mark.parametrize("kernel", ["bulkload", "chunked"])
 @pytest.mark.parametrize("P", [2, 4])
 def test_small_p_with_a_staged_kernel_choice(ddl, kernel, P):
