@@ -263,6 +263,9 @@ def ddl_noalloc_check(stream=None):
 
 # -- convenience object --------------------------------------------------------
 
+_ddl_allreduce = _lib.ddl_allreduce
+_NO_STREAM = object()  # no stream object seen yet (None means the current stream, looked up each call)
+
 TOPOLOGIES = {"ring": DDL_RING, "multiring": DDL_MULTIRING, "torus": DDL_TORUS, "torus_nd": DDL_RING}
 DTYPES = {"f32": DDL_FP32, "f16": DDL_FP16}
 MODES = {"fused": DDL_MODE_FUSED, "stepwise": DDL_MODE_STEPWISE, "rankorder": DDL_MODE_RANKORDER}
@@ -277,6 +280,7 @@ class Plan:
                  mode="fused", kernel="auto", dims=None):
         self.P, self.N, self.dtype = int(P), int(N), dtype
         self._last_ptrs, self._last_arr = None, None
+        self._last_stream, self._last_handle = _NO_STREAM, None
         topo_t = ddl_topology_t(TOPOLOGIES[topo], int(k), int(X), int(Y))
         self.handle = ddl_plan_create(self.P, self.N, DTYPES[dtype], topo_t, int(bucket_bytes))
         try:
@@ -299,11 +303,22 @@ class Plan:
                    layers=w.layers, dims=getattr(w, "dims", None), **kw)
 
     def allreduce(self, rank_bufs, scale, stream=None):
-        # the ctypes pointer array is rebuilt only when the buffers change
-        ptrs = tuple(_dev_ptrs(rank_bufs))
+        # the per-call path of small all-reduces: the ctypes pointer array is
+        # rebuilt only when the buffers change, and the stream handle is kept
+        # for the stream object last seen
+        try:
+            ptrs = [b.data_ptr() for b in rank_bufs]
+        except AttributeError:
+            ptrs = _dev_ptrs(rank_bufs)
         if ptrs != self._last_ptrs:
             self._last_ptrs, self._last_arr = ptrs, _ptr_array(ptrs)
-        _ok(_lib.ddl_allreduce(self.handle, self._last_arr, scale, _stream_handle(stream)), "ddl_allreduce")
+        if stream is None or stream is not self._last_stream:
+            self._last_stream, self._last_handle = stream, _stream_handle(stream)
+            if stream is None:
+                self._last_stream = _NO_STREAM
+        status = _ddl_allreduce(self.handle, self._last_arr, scale, self._last_handle)
+        if status:
+            raise DDLError(status, "ddl_allreduce")
 
     def allreduce_sgd(self, grad_bufs, param_bufs, mom_bufs, scale, lr, momentum=0.0, weight_decay=0.0,
                       keep_grads=True, stream=None):
