@@ -808,6 +808,106 @@ __global__ void __launch_bounds__(kThreads, 2) fold_nd_h2_kernel(const __grid_co
 }
 
 // ---------------------------------------------------------------------------
+// Latency pass of the n-D torus: small items (at most 4 KB per rank) of n-D
+// plans with at least 32 ranks whose P tiles fit in shared memory.  As the
+// two-level latency pass above, the CTA loads all P ranks' columns of its item
+// into shared memory at once, then folds the d levels of the n-D schedule:
+// level 0 groups lev[0] consecutive fold positions, level l groups lev[l]
+// totals of level l-1.  All groups of a level are folded at once, a thread per
+// group and column, and a group's total goes into the shared-memory slot of
+// its first member, which no other group reads (totals below the top are
+// binary16 values where hops are rounded, so they keep their storage form).
+// Every add is rounded to binary16 where a hop would carry it -- all but the
+// final add, the last one at the highest level of size > 1 -- as in the n-D
+// register pass.  The result is stored to every rank from shared memory.
+// (The two-level plans keep their own pass: with totals kept in binary32 and a
+// fixed two-step fold it measured 0.2-0.35 us faster on them.)
+// Shared memory: P x tile bytes (fold position t at t * tile), then one
+// 16-byte result per column.
+// ---------------------------------------------------------------------------
+__host__ __device__ constexpr uint32_t lat_nd_smem_bytes(uint32_t P, uint32_t tile) {
+  return P * tile + (tile / 16u) * 16u;
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(kThreads) fold_lat_nd_kernel(const __grid_constant__ FoldParams p) {
+  constexpr int L = F16 ? 8 : 4;  // elements per 16-byte column
+  extern __shared__ __align__(16) unsigned char s_lat[];
+  __shared__ char* s_ptr[kMaxP];
+  Item s_item;
+  griddep_launch_dependents();
+  if (!load_item(p, s_ptr, &s_item)) return;
+  griddep_wait();
+
+  const int P = p.P, nlev = p.nlev, top = p.top;
+  const bool rh = F16 && p.round_hops;
+  const uint32_t T = p.tile_bytes;
+  const uint64_t eb = s_item.begin, ee = eb + s_item.len;
+  const uint64_t vb = (eb + L - 1) / L, ve = ee / L;
+  if (!p.vector_ok || vb >= ve) {
+    for (uint64_t e = eb + threadIdx.x; e < ee; e += kThreads) fold_nd_scalar<F16>(p, s_ptr, e, rh);
+    return;
+  }
+  const uint32_t ncols = (uint32_t)(ve - vb);  // <= T / 16
+  uint4* s_res = reinterpret_cast<uint4*>(s_lat + (size_t)P * T);
+
+  // every fold position's columns, all loads in flight together
+  for (uint32_t i = threadIdx.x; i < (uint32_t)P * ncols; i += kThreads) {
+    const uint32_t t = i / ncols, c = i % ncols;
+    *reinterpret_cast<uint4*>(s_lat + (size_t)t * T + c * 16u) =
+        __ldcs(reinterpret_cast<const uint4*>(s_ptr[t]) + vb + c);
+  }
+  __syncthreads();
+
+  // the levels, innermost first; members of a level-l group sit `stride`
+  // slots apart
+  int stride = 1;
+  for (int l = 0; l < nlev; ++l) {
+    const int D = (int)p.lev[l];
+    if (D > 1) {
+      const uint32_t ng = (uint32_t)(P / (stride * D));  // one group at the top level
+      for (uint32_t i = threadIdx.x; i < ng * ncols; i += kThreads) {
+        const uint32_t g = i / ncols, c = i % ncols;
+        const size_t first = (size_t)g * (size_t)D * (size_t)stride;
+        float a[L];
+        unpack<F16>(*reinterpret_cast<const uint4*>(s_lat + first * T + c * 16u), a);
+        for (int m = 1; m < D; ++m) {
+          float f[L];
+          unpack<F16>(*reinterpret_cast<const uint4*>(s_lat + (first + (size_t)m * stride) * T + c * 16u), f);
+          const bool round = rh && !(l == top && m == D - 1);
+#pragma unroll
+          for (int q = 0; q < L; ++q) {
+            const float v = __fadd_rn(a[q], f[q]);
+            a[q] = round ? round_h(v) : v;
+          }
+        }
+        if (l == top) {  // the final value: scaled, in storage form
+#pragma unroll
+          for (int q = 0; q < L; ++q) a[q] = __fmul_rn(a[q], p.scale);
+          s_res[c] = pack<F16>(a);
+        } else {         // a total below the top: exact in storage form
+          *reinterpret_cast<uint4*>(s_lat + first * T + c * 16u) = pack<F16>(a);
+        }
+      }
+      __syncthreads();
+    }
+    stride *= D;
+  }
+
+  // the result to every rank, all threads at once
+  for (uint32_t i = threadIdx.x; i < (uint32_t)P * ncols; i += kThreads) {
+    const uint32_t t = i / ncols, c = i % ncols;
+    __stcs(reinterpret_cast<uint4*>(s_ptr[t]) + vb + c, s_res[c]);
+  }
+  // the few elements of a cut column at either end of the item
+  const uint64_t nh = vb * L - eb, nt = ee - ve * L;
+  if (threadIdx.x < nh + nt) {
+    const uint64_t e = threadIdx.x < nh ? eb + threadIdx.x : ve * L + (threadIdx.x - nh);
+    fold_nd_scalar<F16>(p, s_ptr, e, rh);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // The bulk-load pass: shared-memory staged, with bulk asynchronous loads,
 // warp-specialised.
 //
@@ -1322,19 +1422,44 @@ cudaError_t launch_items(void (*kernel)(FoldParams), const FoldParams& p, uint32
 constexpr int kLatMinP = DDL_LAT_MIN_P;
 constexpr uint32_t kLatMaxSmem = 96u * 1024u;
 
-template <bool F16>
-cudaError_t launch_lat(const FoldParams& p, uint32_t n_items, cudaStream_t stream, bool early, uint32_t smem) {
-  // the opt-in above 48 KB, once per device
-  static int ready[64];
+// The n-D latency pass's conditions: aligned buffers, items of at most 4 KB
+// per rank, P >= kLatMinP, levels that cover the P ranks, the tiles within
+// kLatMaxSmem.
+bool lat_nd_applies(const FoldParams& p) {
+  if (!p.vector_ok || p.tile_bytes > (uint32_t)kThreads * 16u || p.P < kLatMinP) return false;
+  if (p.nlev < 1 || p.nlev > kMaxDims || p.top < 0 || p.top >= p.nlev) return false;
+  int64_t prod = 1;
+  for (int l = 0; l < p.nlev; ++l) prod *= p.lev[l];
+  return prod == p.P && lat_nd_smem_bytes((uint32_t)p.P, p.tile_bytes) <= kLatMaxSmem;
+}
+
+// The opt-in above 48 KB of shared memory, once per kernel and device.
+cudaError_t lat_smem_opt_in(void (*kernel)(FoldParams), int* ready) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!ready[dev]) {
-    e = cudaFuncSetAttribute(fold_lat_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLatMaxSmem);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLatMaxSmem);
     if (e != cudaSuccess) return e;
     ready[dev] = 1;
   }
+  return cudaSuccess;
+}
+
+template <bool F16>
+cudaError_t launch_lat_nd(const FoldParams& p, uint32_t n_items, cudaStream_t stream, bool early) {
+  static int ready[64];
+  const cudaError_t e = lat_smem_opt_in(fold_lat_nd_kernel<F16>, ready);
+  if (e != cudaSuccess) return e;
+  return launch_items(fold_lat_nd_kernel<F16>, p, n_items, stream, early, lat_nd_smem_bytes((uint32_t)p.P, p.tile_bytes));
+}
+
+template <bool F16>
+cudaError_t launch_lat(const FoldParams& p, uint32_t n_items, cudaStream_t stream, bool early, uint32_t smem) {
+  static int ready[64];
+  const cudaError_t e = lat_smem_opt_in(fold_lat_kernel<F16>, ready);
+  if (e != cudaSuccess) return e;
   return launch_items(fold_lat_kernel<F16>, p, n_items, stream, early, smem);
 }
 
@@ -1374,6 +1499,9 @@ cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaS
 cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream,
                         bool early_launch) {
   if (n_items == 0) return cudaSuccess;
+  if (p.nlev > 0 && variant == kVarLdg && lat_nd_applies(p))  // n-D torus, small items of many ranks
+    return f16 ? launch_lat_nd<true>(p, n_items, stream, early_launch)
+               : launch_lat_nd<false>(p, n_items, stream, early_launch);
   if (p.nlev > 0) {  // n-D torus: the level-cascade register pass
     // two columns per thread (items up to 8 KB); fp16 with rounded hops folds
     // packed pairs, fp16 without them (unused by the plans) one column (4 KB)

@@ -187,9 +187,10 @@ def test_allreduce_sgd_matches_oracle(ddl, case, mom, keep):
 
 
 # Small buffers (items of 1-4 KB per rank): P >= 32 takes the latency pass
-# (shared-memory staged, row groups folded in parallel) while its tiles fit in
-# 96 KB; smaller single-group unrounded folds take the small-item pass; the
-# rest the register pass.  N is odd, so items end in cut columns.
+# (shared-memory staged, the fold's levels folded group by group in
+# parallel; 2D and n-D tori) while its tiles fit in 96 KB; smaller
+# single-group unrounded folds take the small-item pass; the rest the
+# register passes.  N is odd, so items end in cut columns.
 SMALL_BUFFERS = [
     dict(P=32, N=40_001, topo="torus", X=8, Y=4),
     dict(P=32, N=9_999, topo="torus", X=4, Y=8),
@@ -202,6 +203,12 @@ SMALL_BUFFERS = [
     dict(P=40, N=5_001, layers=[1_000, 2_001, 2_000], bucket_bytes=4_000),
     dict(P=8, N=40_001, topo="multiring", k=2),
     dict(P=12, N=30_001, topo="torus", X=4, Y=3),
+    dict(P=64, N=20_001, topo="torus_nd", dims=[4, 4, 4]),
+    dict(P=32, N=30_003, topo="torus_nd", dims=[4, 4, 2]),
+    dict(P=32, N=12_345, topo="torus_nd", dims=[2, 4, 4]),
+    dict(P=32, N=9_001, topo="torus_nd", dims=[4, 1, 8]),
+    dict(P=32, N=20_001, topo="torus_nd", dims=[8, 4]),
+    dict(P=48, N=30_001, topo="torus_nd", dims=[2, 3, 2, 4], bucket_bytes=50_000),
 ]
 
 
