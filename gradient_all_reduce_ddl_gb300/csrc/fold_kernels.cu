@@ -1433,6 +1433,33 @@ bool lat_nd_applies(const FoldParams& p) {
   return prod == p.P && lat_nd_smem_bytes((uint32_t)p.P, p.tile_bytes) <= kLatMaxSmem;
 }
 
+// The current device's SM count, looked up once per device (GB300's 152 if the
+// query fails).
+uint32_t sm_count() {
+  static int sms[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 152;
+  }
+  if (!sms[dev] && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152;
+  }
+  return (uint32_t)sms[dev];
+}
+
+// CTAs of the latency pass that fit on the GPU at once with `smem` bytes of
+// dynamic shared memory each (plus the 2 KB rank-pointer table, and 1 KB the
+// hardware keeps per CTA; at most 8 CTAs of kThreads per SM).
+uint32_t lat_wave(uint32_t smem) {
+  const uint32_t per_sm_bytes = 228u * 1024u;
+  uint32_t per_sm = per_sm_bytes / (smem + 3u * 1024u);
+  if (per_sm > 8u) per_sm = 8u;
+  if (per_sm < 1u) per_sm = 1u;
+  return per_sm * sm_count();
+}
+
 // The opt-in above 48 KB of shared memory, once per kernel and device.
 cudaError_t lat_smem_opt_in(void (*kernel)(FoldParams), int* ready) {
   int dev = 0;
@@ -1469,15 +1496,21 @@ cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t strea
   // is refused (the element-wise path, taken for unaligned buffers, covers
   // any item)
   if (p.vector_ok && p.tile_bytes > (uint32_t)kTileBytes) return cudaErrorInvalidValue;
-  // small items of many ranks: the latency pass
+  // small items of many ranks: the latency pass -- except for a single
+  // unrounded group whose items need more than one wave of it, where the
+  // small-item pass's occupancy wins (P = 64 multi-ring, 3 latency CTAs per SM:
+  // 409 items 16.6 against 18.4 us per all-reduce, 646 items 26.0 against
+  // 20.5 us)
+  const bool unrounded = !F16 || !p.round_hops;
+  const bool single = unrounded && p.groups == 1 && p.inner == p.P;
   if (p.vector_ok && p.tile_bytes <= (uint32_t)kThreads * 16u && p.P >= kLatMinP && p.groups >= 1 &&
       p.inner >= 1 && (int64_t)p.inner * p.groups == p.P) {
     const uint32_t smem = lat_smem_bytes((uint32_t)p.P, (uint32_t)p.groups, p.tile_bytes, F16 ? 8u : 4u);
-    if (smem <= kLatMaxSmem) return launch_lat<F16>(p, n_items, stream, early, smem);
+    if (smem <= kLatMaxSmem && (!single || n_items <= lat_wave(smem)))
+      return launch_lat<F16>(p, n_items, stream, early, smem);
   }
   // small items of a single unrounded group: the small-item pass (one column
   // per thread covers up to kThreads * 16 bytes per rank)
-  const bool unrounded = !F16 || !p.round_hops;
   if (unrounded && p.groups == 1 && p.inner == p.P && p.tile_bytes <= (uint32_t)kThreads * 16u)
     return launch_items(fold_small_kernel<F16>, p, n_items, stream, early);
   if constexpr (F16) {
