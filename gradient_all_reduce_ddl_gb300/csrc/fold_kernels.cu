@@ -17,6 +17,7 @@
 // so the compiler cannot contract or reorder them.
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "kernels.h"
@@ -1434,19 +1435,23 @@ bool lat_nd_applies(const FoldParams& p) {
 }
 
 // The current device's SM count, looked up once per device (GB300's 152 if the
-// query fails).
+// query fails).  Threads may launch at once: the cache is atomic.
 uint32_t sm_count() {
-  static int sms[64];
+  static std::atomic<int> sms[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     cudaGetLastError();
     return 152;
   }
-  if (!sms[dev] && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    cudaGetLastError();
-    return 152;
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return 152;
+    }
+    sms[dev].store(n, std::memory_order_relaxed);
   }
-  return (uint32_t)sms[dev];
+  return (uint32_t)n;
 }
 
 // CTAs of the latency pass that fit on the GPU at once with `smem` bytes of
@@ -1460,23 +1465,24 @@ uint32_t lat_wave(uint32_t smem) {
   return per_sm * sm_count();
 }
 
-// The opt-in above 48 KB of shared memory, once per kernel and device.
-cudaError_t lat_smem_opt_in(void (*kernel)(FoldParams), int* ready) {
+// The opt-in above 48 KB of shared memory, once per kernel and device (the
+// attribute call is idempotent, so two threads that race here both succeed).
+cudaError_t lat_smem_opt_in(void (*kernel)(FoldParams), std::atomic<bool>* ready) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!ready[dev]) {
+  if (!ready[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLatMaxSmem);
     if (e != cudaSuccess) return e;
-    ready[dev] = 1;
+    ready[dev].store(true, std::memory_order_release);
   }
   return cudaSuccess;
 }
 
 template <bool F16>
 cudaError_t launch_lat_nd(const FoldParams& p, uint32_t n_items, cudaStream_t stream, bool early) {
-  static int ready[64];
+  static std::atomic<bool> ready[64];
   const cudaError_t e = lat_smem_opt_in(fold_lat_nd_kernel<F16>, ready);
   if (e != cudaSuccess) return e;
   return launch_items(fold_lat_nd_kernel<F16>, p, n_items, stream, early, lat_nd_smem_bytes((uint32_t)p.P, p.tile_bytes));
@@ -1484,7 +1490,7 @@ cudaError_t launch_lat_nd(const FoldParams& p, uint32_t n_items, cudaStream_t st
 
 template <bool F16>
 cudaError_t launch_lat(const FoldParams& p, uint32_t n_items, cudaStream_t stream, bool early, uint32_t smem) {
-  static int ready[64];
+  static std::atomic<bool> ready[64];
   const cudaError_t e = lat_smem_opt_in(fold_lat_kernel<F16>, ready);
   if (e != cudaSuccess) return e;
   return launch_items(fold_lat_kernel<F16>, p, n_items, stream, early, smem);
