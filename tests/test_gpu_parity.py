@@ -1000,6 +1000,57 @@ def test_two_plans_on_two_streams_concurrently(ddl):
             assert np.array_equal(to_numpy_bits(bufs[r]), ref3[r]), (w.topo, r)
 
 
+def test_plans_driven_from_several_host_threads(ddl):
+    """Four host threads, each creating its own plan and stream and running
+    five all-reduces on its own buffers, all at once (the binding releases the
+    interpreter lock during library calls).  The plans cover the register
+    pass, the small-item pass and the latency pass (P >= 32, the first launch
+    of it on the device among them), so the library's per-device launch
+    caches are filled concurrently.  Every result matches five applications of
+    the oracle."""
+    import threading
+    ws = [_w(P=16, N=300_001, topo="torus", X=4, Y=4, seed=81),
+          _w(P=32, N=16_384, dtype="f16", topo="torus", X=8, Y=4, seed=82),
+          _w(P=64, N=9_001, topo="multiring", k=4, seed=83),
+          _w(P=4, N=65_536, dist="int1000", scale=1.0, seed=84)]
+    reps = 5
+    inputs = [_host_inputs(w) for w in ws]
+    bufs = [device_bufs_from_host(h, DEV) for h in inputs]
+    torch.cuda.synchronize()
+    errors = [None] * len(ws)
+    start = threading.Barrier(len(ws))
+
+    def run(i):
+        try:
+            s = torch.cuda.Stream(DEV)
+            s.wait_stream(torch.cuda.default_stream(DEV))
+            with ddl.Plan.for_workload(ws[i]) as plan:
+                start.wait(timeout=60)
+                for _ in range(reps):
+                    plan.allreduce(bufs[i], ws[i].scale, stream=s)
+                s.synchronize()
+                plan.check()
+        except BaseException as e:  # reported on the main thread
+            errors[i] = e
+            start.abort()  # the others stop waiting at the barrier
+
+    threads = [threading.Thread(target=run, args=(i,), daemon=True) for i in range(len(ws))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not any(t.is_alive() for t in threads), "a thread did not finish"
+    for e in errors:
+        if e is not None:
+            raise e
+    for w, host, got in zip(ws, inputs, bufs):
+        ref = [h.copy() for h in host]
+        for _ in range(reps):
+            oracle.emulate(oracle_cfg(w), ref, w.scale)
+        for r in range(w.P):
+            assert np.array_equal(to_numpy_bits(got[r]), ref[r]), (w.topo, w.P, r)
+
+
 def test_allreduce_captured_in_cuda_graph(ddl):
     """After a first (uploading) call, ddl_allreduce can be captured in a CUDA
     graph; each replay reduces whatever the buffers hold at that time."""
