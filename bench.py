@@ -65,9 +65,9 @@ SECONDARY = ("ring4_int", "torus4x4_resnet50", "torus8x4_resnet50_f16", "multiri
 # algorithmic bytes; a changed kernel source reports null.
 NCU_TRAFFIC = {
     # P = 16 x 20,000,000 fp32 (1.28 GB resident, above L2): 2.56 GB algorithmic per launch
-    ("ring", "f32", "ldg", "c71916cf78fd6d80"): (1_280_238_592 + 1_220_634_880, 2_560_000_000),
-    ("multiring", "f32", "ldg", "c71916cf78fd6d80"): (1_280_328_704 + 1_220_625_920, 2_560_000_000),
-    ("torus", "f32", "ldg", "c71916cf78fd6d80"): (1_280_200_704 + 1_220_981_504, 2_560_000_000),
+    ("ring", "f32", "ldg", "09f98e7e4fd55312"): (1_280_214_016 + 1_220_160_256, 2_560_000_000),
+    ("multiring", "f32", "ldg", "09f98e7e4fd55312"): (1_280_200_448 + 1_220_776_704, 2_560_000_000),
+    ("torus", "f32", "ldg", "09f98e7e4fd55312"): (1_280_199_680 + 1_220_691_456, 2_560_000_000),
 }
 
 KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]

@@ -399,16 +399,24 @@ __global__ void __launch_bounds__(kThreads) fold_small_kernel(const __grid_const
 // memory, all threads at once.  The adds, their order and their roundings are
 // exactly those of the register pass: a group is the left fold of its inner
 // ranks, each add rounded to binary16 where a hop would carry it; the group
-// totals are left-folded, every add rounded but the final one.
+// totals are left-folded, every add rounded but the final one.  A single
+// group (SINGLE: the ring and multi-ring folds, and rank order) has no totals
+// to fold: its fold, scaled, is the result, one barrier earlier (per
+// all-reduce in graph replay, P = 64 multi-ring at 4K / 16K elements per rank:
+// 3.07 / 4.51 us, against 3.28 / 4.72 us through the totals phase).
 // Shared memory: P x tile bytes of data (fold position t at t * tile), then
-// groups x columns binary32 group totals (L lanes each), then one 16-byte
-// result per column.
+// the binary32 group totals, then one 16-byte result per column.  The totals
+// are 16-byte slices of 4 lanes: slice q of group g sits in row g * L/4 + q,
+// one 16-byte column per thread, so a warp's threads touch consecutive 16
+// bytes.  Stored one binary32 lane at a time, L lanes apart, they conflicted
+// 4- to 8-way in the shared-memory banks (8x4 fp16 torus at 4K / 16K / 64K
+// elements: 3.29 / 5.33 / 5.75 us then, 3.08 / 4.73 / 5.21 us now).
 // ---------------------------------------------------------------------------
 __host__ __device__ constexpr uint32_t lat_smem_bytes(uint32_t P, uint32_t groups, uint32_t tile, uint32_t lanes) {
   return P * tile + groups * (tile / 16u) * lanes * 4u + (tile / 16u) * 16u;
 }
 
-template <bool F16>
+template <bool F16, bool SINGLE>
 __global__ void __launch_bounds__(kThreads) fold_lat_kernel(const __grid_constant__ FoldParams p) {
   constexpr int L = F16 ? 8 : 4;  // elements per 16-byte column
   extern __shared__ __align__(16) unsigned char s_lat[];
@@ -429,8 +437,10 @@ __global__ void __launch_bounds__(kThreads) fold_lat_kernel(const __grid_constan
     return;
   }
   const uint32_t ncols = (uint32_t)(ve - vb);  // <= T / 16
-  float* s_tot = reinterpret_cast<float*>(s_lat + (size_t)P * T);
-  uint4* s_res = reinterpret_cast<uint4*>(s_lat + (size_t)P * T + (size_t)groups * (T / 16u) * L * 4u);
+  // the group totals' 4-lane slices: row g * L/4 + q, CT columns per row
+  const uint32_t CT = T / 16u;
+  float4* s_tot = reinterpret_cast<float4*>(s_lat + (size_t)P * T);
+  uint4* s_res = reinterpret_cast<uint4*>(s_lat + (size_t)P * T + (size_t)groups * CT * L * 4u);
 
   // every fold position's columns, all loads in flight together
   for (uint32_t i = threadIdx.x; i < (uint32_t)P * ncols; i += kThreads) {
@@ -463,30 +473,47 @@ __global__ void __launch_bounds__(kThreads) fold_lat_kernel(const __grid_constan
         }
       }
     }
+    if constexpr (SINGLE) {  // one group: its fold is the result
 #pragma unroll
-    for (int l = 0; l < L; ++l) s_tot[((size_t)g * (T / 16u) + c) * L + l] = a[l];
+      for (int l = 0; l < L; ++l) a[l] = __fmul_rn(a[l], p.scale);
+      s_res[c] = pack<F16>(a);
+    } else {
+#pragma unroll
+      for (int q = 0; q < L / 4; ++q)
+        s_tot[((size_t)g * (L / 4) + q) * CT + c] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+    }
   }
   __syncthreads();
 
   // each column: the left fold of its group totals, scaled, in storage form
-  for (uint32_t c = threadIdx.x; c < ncols; c += kThreads) {
-    float o[L];
+  if constexpr (!SINGLE) {
+    for (uint32_t c = threadIdx.x; c < ncols; c += kThreads) {
+      float o[L];
 #pragma unroll
-    for (int l = 0; l < L; ++l) o[l] = s_tot[(size_t)c * L + l];
-    for (int g = 1; g < groups; ++g) {
-      const bool round = rh && g != groups - 1;  // the last group's add is the final one
-#pragma unroll
-      for (int l = 0; l < L; ++l) {
-        const float v = __fadd_rn(o[l], s_tot[((size_t)g * (T / 16u) + c) * L + l]);
-        o[l] = round ? round_h(v) : v;
+      for (int q = 0; q < L / 4; ++q) {
+        const float4 v = s_tot[(size_t)q * CT + c];
+        o[4 * q] = v.x, o[4 * q + 1] = v.y, o[4 * q + 2] = v.z, o[4 * q + 3] = v.w;
       }
-    }
+      for (int g = 1; g < groups; ++g) {
+        const bool round = rh && g != groups - 1;  // the last group's add is the final one
+        float t[L];
 #pragma unroll
-    for (int l = 0; l < L; ++l) o[l] = __fmul_rn(o[l], p.scale);
-    s_res[c] = pack<F16>(o);
+        for (int q = 0; q < L / 4; ++q) {
+          const float4 v = s_tot[((size_t)g * (L / 4) + q) * CT + c];
+          t[4 * q] = v.x, t[4 * q + 1] = v.y, t[4 * q + 2] = v.z, t[4 * q + 3] = v.w;
+        }
+#pragma unroll
+        for (int l = 0; l < L; ++l) {
+          const float v = __fadd_rn(o[l], t[l]);
+          o[l] = round ? round_h(v) : v;
+        }
+      }
+#pragma unroll
+      for (int l = 0; l < L; ++l) o[l] = __fmul_rn(o[l], p.scale);
+      s_res[c] = pack<F16>(o);
+    }
+    __syncthreads();
   }
-  __syncthreads();
-
   // the result to every rank, all threads at once
   for (uint32_t i = threadIdx.x; i < (uint32_t)P * ncols; i += kThreads) {
     const uint32_t t = i / ncols, c = i % ncols;
@@ -1490,10 +1517,12 @@ cudaError_t launch_lat_nd(const FoldParams& p, uint32_t n_items, cudaStream_t st
 
 template <bool F16>
 cudaError_t launch_lat(const FoldParams& p, uint32_t n_items, cudaStream_t stream, bool early, uint32_t smem) {
-  static std::atomic<bool> ready[64];
-  const cudaError_t e = lat_smem_opt_in(fold_lat_kernel<F16>, ready);
+  static std::atomic<bool> ready[2][64];
+  const bool single = p.groups == 1;
+  void (*const kernel)(FoldParams) = single ? fold_lat_kernel<F16, true> : fold_lat_kernel<F16, false>;
+  const cudaError_t e = lat_smem_opt_in(kernel, ready[single ? 1 : 0]);
   if (e != cudaSuccess) return e;
-  return launch_items(fold_lat_kernel<F16>, p, n_items, stream, early, smem);
+  return launch_items(kernel, p, n_items, stream, early, smem);
 }
 
 template <bool F16>
