@@ -145,7 +145,8 @@ void set_levels(const ddl_plan* p, ddl::FoldParams* fp) {
 // Work-item size for the plan's kernel: the n-D pass covers 8 KB (fp32) or
 // 4 KB (fp16) per rank per CTA; the staged passes fill ~64 KB per stage.
 uint32_t choose_tile(const Spec& s, int kernel) {
-  const uint32_t ldg = ddl::ldg_tile_bytes(s.N * (uint64_t)s.esize);
+  const uint32_t ldg =
+      ddl::ldg_tile_bytes(s.N * (uint64_t)s.esize, ddl::fused_tile_floor(s.P, s.topo, s.Y, s.esize, s.mode));
   if (s.topo == ddl::kTorusND) {
     // the n-D pass's columns per thread: two, except fp16 without rounded hops
     const uint32_t cap = (s.esize == 2 && s.mode != ddl::kFused) ? 4096u : 8192u;
@@ -348,7 +349,7 @@ ddl_status_t ddl_plan_create(int P, size_t N, ddl_dtype_t dtype, ddl_topology_t 
   s.X = topo.kind == DDL_TORUS ? topo.X : 0;
   s.Y = topo.kind == DDL_TORUS ? topo.Y : 0;
   s.bucket_bytes = bucket_bytes;
-  s.tile_bytes = ddl::ldg_tile_bytes((uint64_t)N * (uint64_t)(s.esize ? s.esize : 4));
+  s.tile_bytes = choose_tile(s, DDL_KERNEL_AUTO);
   bool unsupported = false;
   const std::string why = ddl::validate(s, &unsupported);
   if (!why.empty()) return unsupported ? DDL_ERR_UNSUPPORTED : DDL_ERR_INVALID_ARG;
@@ -383,6 +384,7 @@ ddl_status_t ddl_plan_set_mode(ddl_plan_t p, ddl_mode_t mode) {
   if ((int)mode == p->spec.mode) return DDL_OK;
   const Spec old = p->spec;
   p->spec.mode = (int)mode;
+  p->spec.tile_bytes = choose_tile(p->spec, p->kernel);  // the floor follows the fold shape
   const ddl_status_t st = rebuild(p);
   if (st != DDL_OK) {
     p->spec = old;

@@ -1438,16 +1438,13 @@ cudaError_t launch_items(void (*kernel)(FoldParams), const FoldParams& p, uint32
 }
 
 // The latency pass takes small items (at most 4 KB per rank) of plans with at
-// least kLatMinP ranks whose shared-memory footprint stays within kLatMaxSmem.
-// Measured per all-reduce in graph replay: at P = 32 (8x4 fp16 torus, 16,384
-// elements per rank) 5.33 us against 7.18 us in the register pass, at P = 64
-// (4-ring multi-ring, fp32) 4.72 against 8.62 us; at P = 16 its three barriers
-// cost more than the register pass's two batches of loads (ring 3.20 against
-// 3.07 us), so smaller plans keep the register or small-item pass.
-#ifndef DDL_LAT_MIN_P
-#define DDL_LAT_MIN_P 32
-#endif
-constexpr int kLatMinP = DDL_LAT_MIN_P;
+// least kLatMinP ranks (plan.h) whose shared-memory footprint stays within
+// kLatMaxSmem.  Measured per all-reduce in graph replay, with 1 KB items: at
+// P = 32 (8x4 fp16 torus, 16,384 elements per rank) 5.33 us against 7.18 us in
+// the register pass, at P = 64 (4-ring multi-ring, fp32) 4.72 against 8.62 us;
+// at P = 16 its three barriers cost more than the register pass's two batches
+// of loads (ring 3.20 against 3.07 us), so smaller plans keep the register or
+// small-item pass.
 constexpr uint32_t kLatMaxSmem = 96u * 1024u;
 
 // The n-D latency pass's conditions: aligned buffers, items of at most 4 KB

@@ -181,7 +181,9 @@ extern "C" ddl_status_t ddl_allreduce_noalloc(int P, size_t N, ddl_dtype_t dtype
   sh.mode = ddl::kFused;
   bool unsupported = false;
   if (ddl::check_shape(sh, &unsupported)) return unsupported ? DDL_ERR_UNSUPPORTED : DDL_ERR_INVALID_ARG;
-  sh.tile_bytes = ddl::ldg_tile_bytes(sh.N * (uint64_t)sh.esize);  // N * esize <= 2^40 here
+  // N * esize <= 2^40 here
+  sh.tile_bytes = ddl::ldg_tile_bytes(sh.N * (uint64_t)sh.esize,
+                                      ddl::fused_tile_floor(sh.P, sh.topo, sh.Y, sh.esize, sh.mode));
 
   // sizes first: a problem whose tables exceed the static array is refused
   // before anything is touched (the count stops at the first table that

@@ -375,10 +375,17 @@ struct Builder {
 
 }  // namespace
 
-uint32_t ldg_tile_bytes(uint64_t bytes_per_rank) {
+uint32_t ldg_tile_bytes(uint64_t bytes_per_rank, uint32_t floor) {
   uint32_t t = kTileBytes;
-  while (t > 1024 && bytes_per_rank < (uint64_t)t * 304) t >>= 1;
+  while (t > floor && bytes_per_rank < (uint64_t)t * 304) t >>= 1;
   return t;
+}
+
+uint32_t fused_tile_floor(int P, int topo, int Y, int esize, int mode) {
+  if (P >= kLatMinP) return 256;
+  const bool one_group = mode == kRankOrder || topo == kRing || topo == kMultiRing || (topo == kTorus && Y == 1);
+  const bool unrounded = mode == kRankOrder || esize == 4;
+  return one_group && unrounded ? 256 : 1024;
 }
 
 uint32_t bulk_tile_bytes(int P) {

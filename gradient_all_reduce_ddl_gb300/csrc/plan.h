@@ -81,10 +81,25 @@ struct Spec {
 // pipeline stage fill about 64 KB, between 256 B and kTileBytes per rank.
 uint32_t bulk_tile_bytes(int P);
 
-// Work-item size of the register pass: kTileBytes, or smaller (down to 1 KB)
-// when a rank's buffer is too small to give every SM of a large GPU
-// (2 x 152 items) work at that size.
-uint32_t ldg_tile_bytes(uint64_t bytes_per_rank);
+// Plans of at least this many ranks fold small buffers in the latency pass
+// (all P ranks' columns of a work item staged in shared memory at once).
+#ifndef DDL_LAT_MIN_P
+#define DDL_LAT_MIN_P 32
+#endif
+constexpr int kLatMinP = DDL_LAT_MIN_P;
+
+// Work-item size of the register, small-item and latency passes: kTileBytes,
+// or smaller, down to `floor` bytes, when a rank's buffer is too small to give
+// every SM of a large GPU (2 x 152 items) work at that size.
+uint32_t ldg_tile_bytes(uint64_t bytes_per_rank, uint32_t floor);
+
+// That floor for a plan: 256 bytes where small buffers take the latency pass
+// (P >= kLatMinP) or the small-item pass (a single fold group with no
+// intermediate rounding: rank order, and the binary32 ring, multi-ring and
+// one-row torus), whose time falls with the bytes one CTA stages; 1 KB where
+// they take the register pass, whose fixed costs per CTA then dominate.
+// Y: the torus's rows (ignored for other schedules).
+uint32_t fused_tile_floor(int P, int topo, int Y, int esize, int mode);
 
 struct Tables {
   std::vector<Bucket> buckets;
