@@ -65,9 +65,9 @@ SECONDARY = ("ring4_int", "torus4x4_resnet50", "torus8x4_resnet50_f16", "multiri
 # algorithmic bytes; a changed kernel source reports null.
 NCU_TRAFFIC = {
     # P = 16 x 20,000,000 fp32 (1.28 GB resident, above L2): 2.56 GB algorithmic per launch
-    ("ring", "f32", "ldg", "acb3d38ce701b3e3"): (1_280_198_656 + 1_220_262_400, 2_560_000_000),
-    ("multiring", "f32", "ldg", "acb3d38ce701b3e3"): (1_280_199_424 + 1_220_260_608, 2_560_000_000),
-    ("torus", "f32", "ldg", "acb3d38ce701b3e3"): (1_280_210_944 + 1_220_936_192, 2_560_000_000),
+    ("ring", "f32", "ldg", "a5c9116baf5c54bd"): (1_280_205_056 + 1_220_297_216, 2_560_000_000),
+    ("multiring", "f32", "ldg", "a5c9116baf5c54bd"): (1_280_261_632 + 1_221_012_480, 2_560_000_000),
+    ("torus", "f32", "ldg", "a5c9116baf5c54bd"): (1_280_363_264 + 1_220_453_376, 2_560_000_000),
 }
 
 KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]

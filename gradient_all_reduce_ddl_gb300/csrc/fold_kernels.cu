@@ -158,22 +158,42 @@ __device__ __forceinline__ void store_elem(char* base, uint64_t e, float v) {
   }
 }
 
-// Element-wise path: segment edges that cut a 16-byte column, and buffers
-// that are not 16-byte aligned.
-template <bool F16>
-__device__ void fold_scalar(char* const* ptr, uint64_t e, int P, int inner, int groups, bool rh, float scale) {
+// The element-wise fold at element e: rank position t's buffer is at(t).  Its
+// loads go out eight positions at a time, so an element costs P/8 dependent
+// round trips rather than P (the fold, its order and its roundings are those
+// of the column passes).  Returns the folded value before the scale.
+template <bool F16, class At>
+__device__ __forceinline__ float fold_elem(At at, uint64_t e, int P, int inner, int groups, bool rh) {
   float in = 0.f, out = 0.f;
   int h = 0, g = 0;
-  for (int t = 0; t < P; ++t) {
-    const float v = load_elem<F16>(ptr[t], e);
-    const Ctl c = ctl_at(t, h, g, inner, groups, P, rh);
-    fold_lanes<1>(&in, &out, &v, c);
-    if (++h == inner) {
-      h = 0;
-      ++g;
+  for (int t0 = 0; t0 < P; t0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (t0 + j < P) v[j] = load_elem<F16>(at(t0 + j), e);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (t0 + j < P) {
+        const Ctl c = ctl_at(t0 + j, h, g, inner, groups, P, rh);
+        fold_lanes<1>(&in, &out, &v[j], c);
+        if (++h == inner) {
+          h = 0;
+          ++g;
+        }
+      }
     }
   }
-  const float r = __fmul_rn(out, scale);
+  return out;
+}
+
+// Element-wise path: segment edges that cut a 16-byte column, and buffers
+// that are not 16-byte aligned.  Kept out of line: inlined, its batched loads
+// took registers from the column passes around it and slowed their small
+// buffers (P = 16 ring at 16K elements 2.45 against 2.26 us per all-reduce).
+template <bool F16>
+__device__ __noinline__ void fold_scalar(char* const* ptr, uint64_t e, int P, int inner, int groups, bool rh,
+                                         float scale) {
+  const float r = __fmul_rn(fold_elem<F16>([ptr](int t) { return ptr[t]; }, e, P, inner, groups, rh), scale);
   for (int t = 0; t < P; ++t) store_elem<F16>(ptr[t], e, r);
 }
 
@@ -659,11 +679,16 @@ struct CascadeH2 {
 };
 
 template <bool F16>
-__device__ __forceinline__ void fold_nd_scalar(const FoldParams& p, char* const* ptr, uint64_t e, bool rh) {
+__device__ __noinline__ void fold_nd_scalar(const FoldParams& p, char* const* ptr, uint64_t e, bool rh) {
   Cascade<1> cs;
-  for (int t = 0; t < p.P; ++t) {
-    const float v = load_elem<F16>(ptr[t], e);
-    cs.push(&v, t == p.P - 1, p, rh);
+  for (int t0 = 0; t0 < p.P; t0 += 8) {  // loads eight positions at a time
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (t0 + j < p.P) v[j] = load_elem<F16>(ptr[t0 + j], e);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (t0 + j < p.P) cs.push(&v[j], t0 + j == p.P - 1, p, rh);
   }
   float fin;
   cs.result(&fin, p.nlev);
@@ -1043,18 +1068,8 @@ __host__ __device__ constexpr uint32_t bulk_smem_bytes(uint32_t P, uint32_t tile
 template <bool F16>
 __device__ void fold_scalar_ordered(const FoldParams& p, const uint8_t* order, uint64_t e, int inner, int groups,
                                     bool rh) {
-  float in = 0.f, out = 0.f;
-  int h = 0, g = 0;
-  for (int t = 0; t < p.P; ++t) {
-    const float v = load_elem<F16>(static_cast<const char*>(p.bufs[order[t]]), e);
-    const Ctl c = ctl_at(t, h, g, inner, groups, p.P, rh);
-    fold_lanes<1>(&in, &out, &v, c);
-    if (++h == inner) {
-      h = 0;
-      ++g;
-    }
-  }
-  const float r = __fmul_rn(out, p.scale);
+  const auto at = [&p, order](int t) { return static_cast<const char*>(p.bufs[order[t]]); };
+  const float r = __fmul_rn(fold_elem<F16>(at, e, p.P, inner, groups, rh), p.scale);
   for (int t = 0; t < p.P; ++t) store_elem<F16>(static_cast<char*>(p.bufs[order[t]]), e, r);
 }
 
@@ -1439,12 +1454,13 @@ cudaError_t launch_items(void (*kernel)(FoldParams), const FoldParams& p, uint32
 
 // The latency pass takes small items (at most 4 KB per rank) of plans with at
 // least kLatMinP ranks (plan.h) whose shared-memory footprint stays within
-// kLatMaxSmem.  Measured per all-reduce in graph replay, with 1 KB items: at
-// P = 32 (8x4 fp16 torus, 16,384 elements per rank) 5.33 us against 7.18 us in
-// the register pass, at P = 64 (4-ring multi-ring, fp32) 4.72 against 8.62 us;
-// at P = 16 its three barriers cost more than the register pass's two batches
-// of loads (ring 3.20 against 3.07 us), so smaller plans keep the register or
-// small-item pass.
+// kLatMaxSmem.  Measured per all-reduce in graph replay at 16,384 elements per
+// rank: P = 32 (8x4 fp16 torus) 5.33 us against 7.18 us in the register pass
+// (1 KB items), P = 64 (4-ring multi-ring, fp32) 4.72 against 8.62 us; with
+// 256-byte items, P = 16 ring 2.27 against 2.88 us (small-item pass) and 4x4
+// torus 2.33 against 3.17 us (register pass).  Below 16 it is mixed (P = 8:
+// fp16 torus 2.26 against 2.87 us, fp32 torus at 65,536 elements 2.67 against
+// 2.46 us) and at P = 4 it loses (ring 2.05 against 1.64 us).
 constexpr uint32_t kLatMaxSmem = 96u * 1024u;
 
 // The n-D latency pass's conditions: aligned buffers, items of at most 4 KB

@@ -84,7 +84,7 @@ uint32_t bulk_tile_bytes(int P);
 // Plans of at least this many ranks fold small buffers in the latency pass
 // (all P ranks' columns of a work item staged in shared memory at once).
 #ifndef DDL_LAT_MIN_P
-#define DDL_LAT_MIN_P 32
+#define DDL_LAT_MIN_P 16
 #endif
 constexpr int kLatMinP = DDL_LAT_MIN_P;
 
