@@ -65,9 +65,9 @@ SECONDARY = ("ring4_int", "torus4x4_resnet50", "torus8x4_resnet50_f16", "multiri
 # algorithmic bytes; a changed kernel source reports null.
 NCU_TRAFFIC = {
     # P = 16 x 20,000,000 fp32 (1.28 GB resident, above L2): 2.56 GB algorithmic per launch
-    ("ring", "f32", "ldg", "a5c9116baf5c54bd"): (1_280_205_056 + 1_220_297_216, 2_560_000_000),
-    ("multiring", "f32", "ldg", "a5c9116baf5c54bd"): (1_280_261_632 + 1_221_012_480, 2_560_000_000),
-    ("torus", "f32", "ldg", "a5c9116baf5c54bd"): (1_280_363_264 + 1_220_453_376, 2_560_000_000),
+    ("ring", "f32", "ldg", "e1b2ea7f1275826b"): (1_280_196_096 + 1_220_354_048, 2_560_000_000),
+    ("multiring", "f32", "ldg", "e1b2ea7f1275826b"): (1_280_230_912 + 1_220_017_408, 2_560_000_000),
+    ("torus", "f32", "ldg", "e1b2ea7f1275826b"): (1_280_195_584 + 1_220_519_680, 2_560_000_000),
 }
 
 KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]
@@ -614,7 +614,7 @@ def secondary_leg(ddl, name: str, dev, stream, peak: float, samples: dict, targe
             out = {"P": w.P, "N": w.N, "dtype": w.dtype, "schedule": schedule_name(w), "buckets": plan.num_buckets,
                    "bytes_per_step": w.min_bytes, "steps": steps, "ms_per_step": round(ms, 5),
                    "GBps": round(gbs, 1), "elems_per_s": round(w.P * w.N / (ms * 1e-3), 1),
-                   "frac_of_hbm": round(gbs / peak, 4), "gpu_launches": launches,
+                   "frac_of_hbm": round(gbs / peak, 4), "gpu_launches": launches, "kernel": plan.kernel_name,
                    "l2": ("inputs larger than the 129 MB L2" if w.P * w.N * w.esize > 129e6 else
                           "inputs fit in the 129 MB L2: back-to-back calls run on a warm L2 (latency, not HBM)")}
             if w.P * w.N * w.esize <= 129e6:
@@ -907,9 +907,10 @@ def main():
     kernel_bytes = sum(kernel_bytes_of(p, w, args.mode) for p, w in zip(plans, wls))
     avg_launch_ms = local_ms / (args.steps * launches_per_step)
     achieved = (kernel_bytes / launches_per_step) / (avg_launch_ms * 1e-3) / 1e9
-    kernel_name = {"fused": {"bulkload": "fold_bulk_kernel", "chunked": "fold_chunked_kernel"}.get(
-                                 args.kernel, "fold_nd_kernel" if w0.topo == "torus_nd" else "fold_ldg_kernel"),
-                   "rankorder": "fold_ldg_kernel (rank order)", "stepwise": "step_kernel"}[args.mode]
+    # the kernel the library launches for these plans (its own dispatch rules)
+    kernel_name = " / ".join(dict.fromkeys(p.kernel_name for p in plans))
+    if args.mode == "rankorder":
+        kernel_name += " (rank order)"
     traffic = None
     if args.mode == "fused" and launches_per_step == len(wls):
         per_launch = [ncu_traffic(w, args.kernel, w.min_bytes) for w in wls]

@@ -225,37 +225,45 @@ ddl_status_t check_bufs(ddl_plan* p, void* const* bufs, bool device_check, bool*
   return DDL_OK;
 }
 
+// The launch record of the fused pass over items [ia, ib), and the variant it
+// runs (the plan's kernel choice, or force_variant; the staged passes need
+// 16-byte aligned buffers, else the register pass runs its element-wise path,
+// with the same results).
+int fold_params(const ddl_plan* p, uint32_t ia, uint32_t ib, void* const* bufs, bool aligned, float scale,
+                int force_variant, ddl::FoldParams* fp) {
+  const bool f16 = p->spec.esize == 2;
+  std::memset(fp, 0, sizeof(*fp));
+  fp->items = p->d_items;
+  fp->segs = p->d_segs;
+  fp->orders = p->d_orders;
+  fp->err = p->d_err;
+  fp->item0 = ia;
+  fp->n_segs = (uint32_t)p->tab.segs.size();
+  fp->n_orders = (uint32_t)p->tab.orders.size();
+  fp->P = p->spec.P;
+  fp->scale = scale;
+  fp->round_hops = (f16 && p->spec.mode == ddl::kFused) ? 1 : 0;
+  fp->vector_ok = aligned ? 1 : 0;
+  for (int r = 0; r < p->spec.P; ++r) fp->bufs[r] = bufs ? bufs[r] : nullptr;
+  fp->n_items = ib - ia;
+  fp->tile_bytes = p->spec.tile_bytes;
+  set_levels(p, fp);
+  int variant = ddl::kVarLdg;
+  if (aligned && p->kernel == DDL_KERNEL_BULK_LOAD) variant = ddl::kVarBulkLoad;
+  if (aligned && p->kernel == DDL_KERNEL_CHUNKED) variant = ddl::kVarChunked;
+  if (aligned && force_variant) variant = force_variant;
+  return variant;
+}
+
 // Fused pass over items [ia, ib): a whole bucket, or a tile-aligned element range of one.
 // early: launch as a programmatic dependent of the kernel before it on s (only
 // where nothing but that kernel orders the launch: no event waits, no copies).
 ddl_status_t run_items(ddl_plan* p, uint32_t ia, uint32_t ib, void* const* bufs, bool aligned, float scale,
                        cudaStream_t s, bool early = false, int force_variant = 0) {
   if (ib <= ia) return DDL_OK;
-  const bool f16 = p->spec.esize == 2;
   ddl::FoldParams fp;
-  std::memset(&fp, 0, sizeof(fp));
-  fp.items = p->d_items;
-  fp.segs = p->d_segs;
-  fp.orders = p->d_orders;
-  fp.err = p->d_err;
-  fp.item0 = ia;
-  fp.n_segs = (uint32_t)p->tab.segs.size();
-  fp.n_orders = (uint32_t)p->tab.orders.size();
-  fp.P = p->spec.P;
-  fp.scale = scale;
-  fp.round_hops = (f16 && p->spec.mode == ddl::kFused) ? 1 : 0;
-  fp.vector_ok = aligned ? 1 : 0;
-  for (int r = 0; r < p->spec.P; ++r) fp.bufs[r] = bufs[r];
-  // the staged passes need 16-byte aligned buffers; otherwise the register
-  // pass runs (its element-wise path), with the same results
-  int variant = ddl::kVarLdg;
-  if (aligned && p->kernel == DDL_KERNEL_BULK_LOAD) variant = ddl::kVarBulkLoad;
-  if (aligned && p->kernel == DDL_KERNEL_CHUNKED) variant = ddl::kVarChunked;
-  if (aligned && force_variant) variant = force_variant;
-  fp.n_items = ib - ia;
-  fp.tile_bytes = p->spec.tile_bytes;
-  set_levels(p, &fp);
-  const cudaError_t e = ddl::launch_fold(fp, ib - ia, f16, variant, s, early);
+  const int variant = fold_params(p, ia, ib, bufs, aligned, scale, force_variant, &fp);
+  const cudaError_t e = ddl::launch_fold(fp, ib - ia, p->spec.esize == 2, variant, s, early);
   if (e != cudaSuccess) return cuda_status(e);
   ++p->launches;
   return DDL_OK;
@@ -813,6 +821,20 @@ ddl_status_t ddl_plan_fold_order(ddl_plan_t p, size_t i, int32_t* order, int32_t
 ddl_status_t ddl_plan_launches(ddl_plan_t p, uint64_t* n) {
   if (!p || !n) return DDL_ERR_INVALID_ARG;
   *n = p->launches;
+  return DDL_OK;
+}
+
+ddl_status_t ddl_plan_kernel_name(ddl_plan_t p, const char** name) {
+  if (!p || !name) return DDL_ERR_INVALID_ARG;
+  if (p->spec.mode == ddl::kStepwise) {
+    *name = "step_kernel";
+    return DDL_OK;
+  }
+  // the launch ddl_allreduce makes: one over all of the plan's work items
+  const uint32_t n = (uint32_t)p->tab.items.size();
+  ddl::FoldParams fp;
+  const int variant = fold_params(p, 0, n, nullptr, true, 1.0f, 0, &fp);
+  *name = ddl::fold_pass_kernel(ddl::fold_pass(fp, n, p->spec.esize == 2, variant), fp.round_hops != 0);
   return DDL_OK;
 }
 

@@ -1544,23 +1544,6 @@ cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t strea
   // is refused (the element-wise path, taken for unaligned buffers, covers
   // any item)
   if (p.vector_ok && p.tile_bytes > (uint32_t)kTileBytes) return cudaErrorInvalidValue;
-  // small items of many ranks: the latency pass -- except for a single
-  // unrounded group whose items need more than one wave of it, where the
-  // small-item pass's occupancy wins (P = 64 multi-ring, 3 latency CTAs per SM:
-  // 409 items 16.6 against 18.4 us per all-reduce, 646 items 26.0 against
-  // 20.5 us)
-  const bool unrounded = !F16 || !p.round_hops;
-  const bool single = unrounded && p.groups == 1 && p.inner == p.P;
-  if (p.vector_ok && p.tile_bytes <= (uint32_t)kThreads * 16u && p.P >= kLatMinP && p.groups >= 1 &&
-      p.inner >= 1 && (int64_t)p.inner * p.groups == p.P) {
-    const uint32_t smem = lat_smem_bytes((uint32_t)p.P, (uint32_t)p.groups, p.tile_bytes, F16 ? 8u : 4u);
-    if (smem <= kLatMaxSmem && (!single || n_items <= lat_wave(smem)))
-      return launch_lat<F16>(p, n_items, stream, early, smem);
-  }
-  // small items of a single unrounded group: the small-item pass (one column
-  // per thread covers up to kThreads * 16 bytes per rank)
-  if (unrounded && p.groups == 1 && p.inner == p.P && p.tile_bytes <= (uint32_t)kThreads * 16u)
-    return launch_items(fold_small_kernel<F16>, p, n_items, stream, early);
   if constexpr (F16) {
     if (p.round_hops)
       return launch_items(fold_ldg_kernel<true, true, 2, DDL_LDG_F16_B, DDL_LDG_MINB>, p, n_items, stream, early);
@@ -1570,6 +1553,24 @@ cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t strea
   }
 }
 
+// The n-D torus's level-cascade register pass: two columns per thread (items
+// up to 8 KB); fp16 with rounded hops folds packed pairs, fp16 without them
+// (unused by the plans) one column (4 KB).
+cudaError_t launch_nd(const FoldParams& p, uint32_t n_items, bool f16, cudaStream_t stream, bool early) {
+  if (f16 && p.round_hops) {
+    if (p.nlev < 1 || p.nlev > 4) return cudaErrorInvalidValue;
+    void (*const h2[4])(FoldParams) = {fold_nd_h2_kernel<2, DDL_ND_H2_B1, 1>, fold_nd_h2_kernel<2, DDL_ND_H2_B1, 2>,
+                                       fold_nd_h2_kernel<2, DDL_ND_H2_B3, 3>, fold_nd_h2_kernel<2, DDL_ND_H2_B4, 4>};
+    return launch_items(h2[p.nlev - 1], p, n_items, stream, early);
+  }
+  if (f16) return launch_items(fold_nd_kernel<true, 1, 8>, p, n_items, stream, early);
+  return launch_items(fold_nd_kernel<false, 2, 8>, p, n_items, stream, early);
+}
+
+uint32_t lat_smem_of(const FoldParams& p, bool f16) {
+  return lat_smem_bytes((uint32_t)p.P, (uint32_t)p.groups, p.tile_bytes, f16 ? 8u : 4u);
+}
+
 }  // namespace
 
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream) {
@@ -1577,27 +1578,67 @@ cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaS
   return cudaGetLastError();
 }
 
+FoldPass fold_pass(const FoldParams& p, uint32_t n_items, bool f16, int variant) {
+  if (p.nlev > 0)  // n-D torus: small items of many ranks take its latency pass
+    return variant == kVarLdg && lat_nd_applies(p) ? kPassNdLatency : kPassNdRegister;
+  if (variant == kVarBulkLoad) return kPassBulkLoad;
+  if (variant == kVarChunked) return kPassChunked;
+  // small items of many ranks: the latency pass -- except for a single
+  // unrounded group whose items need more than one wave of it, where the
+  // small-item pass's occupancy wins (P = 64 multi-ring, 3 latency CTAs per SM
+  // with 1 KB items: 409 items 16.6 against 18.4 us per all-reduce, 646 items
+  // 26.0 against 20.5 us)
+  const bool unrounded = !f16 || !p.round_hops;
+  const bool single = unrounded && p.groups == 1 && p.inner == p.P;
+  const bool small_items = p.tile_bytes <= (uint32_t)kThreads * 16u;
+  if (p.vector_ok && small_items && p.P >= kLatMinP && p.groups >= 1 && p.inner >= 1 &&
+      (int64_t)p.inner * p.groups == p.P) {
+    const uint32_t smem = lat_smem_of(p, f16);
+    if (smem <= kLatMaxSmem && (!single || n_items <= lat_wave(smem)))
+      return p.groups == 1 ? kPassLatencySingle : kPassLatency;
+  }
+  // small items of a single unrounded group: the small-item pass (one column
+  // per thread covers up to kThreads * 16 bytes per rank)
+  if (single && small_items) return kPassSmallItem;
+  return kPassRegister;
+}
+
+const char* fold_pass_kernel(FoldPass pass, bool packed_hops) {
+  switch (pass) {
+    case kPassRegister: return "fold_ldg_kernel";
+    case kPassSmallItem: return "fold_small_kernel";
+    case kPassLatency: return "fold_lat_kernel";
+    case kPassLatencySingle: return "fold_lat_kernel (one group)";
+    case kPassNdRegister: return packed_hops ? "fold_nd_h2_kernel" : "fold_nd_kernel";
+    case kPassNdLatency: return "fold_lat_nd_kernel";
+    case kPassBulkLoad: return "fold_bulk_kernel";
+    case kPassChunked: return "fold_chunked_kernel";
+  }
+  return "unknown";
+}
+
 cudaError_t launch_fold(const FoldParams& p, uint32_t n_items, bool f16, int variant, cudaStream_t stream,
                         bool early_launch) {
   if (n_items == 0) return cudaSuccess;
-  if (p.nlev > 0 && variant == kVarLdg && lat_nd_applies(p))  // n-D torus, small items of many ranks
-    return f16 ? launch_lat_nd<true>(p, n_items, stream, early_launch)
-               : launch_lat_nd<false>(p, n_items, stream, early_launch);
-  if (p.nlev > 0) {  // n-D torus: the level-cascade register pass
-    // two columns per thread (items up to 8 KB); fp16 with rounded hops folds
-    // packed pairs, fp16 without them (unused by the plans) one column (4 KB)
-    if (f16 && p.round_hops) {
-      if (p.nlev < 1 || p.nlev > 4) return cudaErrorInvalidValue;
-      void (*const h2[4])(FoldParams) = {fold_nd_h2_kernel<2, DDL_ND_H2_B1, 1>, fold_nd_h2_kernel<2, DDL_ND_H2_B1, 2>,
-                                         fold_nd_h2_kernel<2, DDL_ND_H2_B3, 3>, fold_nd_h2_kernel<2, DDL_ND_H2_B4, 4>};
-      return launch_items(h2[p.nlev - 1], p, n_items, stream, early_launch);
-    }
-    if (f16) return launch_items(fold_nd_kernel<true, 1, 8>, p, n_items, stream, early_launch);
-    return launch_items(fold_nd_kernel<false, 2, 8>, p, n_items, stream, early_launch);
+  switch (fold_pass(p, n_items, f16, variant)) {
+    case kPassNdLatency:
+      return f16 ? launch_lat_nd<true>(p, n_items, stream, early_launch)
+                 : launch_lat_nd<false>(p, n_items, stream, early_launch);
+    case kPassNdRegister:
+      return launch_nd(p, n_items, f16, stream, early_launch);
+    case kPassBulkLoad:
+      return f16 ? launch_bulk<true>(p, n_items, stream) : launch_bulk<false>(p, n_items, stream);
+    case kPassChunked:
+      return f16 ? launch_chunked<true>(p, n_items, stream) : launch_chunked<false>(p, n_items, stream);
+    case kPassLatency:
+    case kPassLatencySingle:
+      return f16 ? launch_lat<true>(p, n_items, stream, early_launch, lat_smem_of(p, true))
+                 : launch_lat<false>(p, n_items, stream, early_launch, lat_smem_of(p, false));
+    case kPassSmallItem:
+      return launch_items(f16 ? fold_small_kernel<true> : fold_small_kernel<false>, p, n_items, stream, early_launch);
+    case kPassRegister:
+      break;
   }
-  if (variant == kVarBulkLoad) return f16 ? launch_bulk<true>(p, n_items, stream) : launch_bulk<false>(p, n_items, stream);
-  if (variant == kVarChunked)
-    return f16 ? launch_chunked<true>(p, n_items, stream) : launch_chunked<false>(p, n_items, stream);
   return f16 ? launch_ldg<true>(p, n_items, stream, early_launch) : launch_ldg<false>(p, n_items, stream, early_launch);
 }
 

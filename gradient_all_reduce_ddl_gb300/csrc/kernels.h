@@ -80,6 +80,25 @@ struct StepParams {
 // (all ranks of a tile per stage), the rank-chunked staged pass.
 enum FoldVariant : int { kVarLdg = 1, kVarBulkLoad = 3, kVarChunked = 4 };
 
+// The pass a fused launch of n_items work items takes.  launch_fold launches
+// exactly this choice; it depends on the plan's shape, the buffers' alignment
+// (p.vector_ok), the variant and, for a single fold group, on how many CTAs of
+// the latency pass fit on the device at once.
+enum FoldPass : int {
+  kPassRegister = 0,   // fold_ldg_kernel
+  kPassSmallItem,      // fold_small_kernel: one unrounded group, small items
+  kPassLatency,        // fold_lat_kernel, several groups
+  kPassLatencySingle,  // fold_lat_kernel, one group
+  kPassNdRegister,     // fold_nd_kernel, fold_nd_h2_kernel (binary16 hops)
+  kPassNdLatency,      // fold_lat_nd_kernel
+  kPassBulkLoad,       // fold_bulk_kernel
+  kPassChunked         // fold_chunked_kernel
+};
+FoldPass fold_pass(const FoldParams& p, uint32_t n_items, bool f16, int variant);
+// The kernel's name (a static string); packed_hops: binary16 storage with
+// rounded hops.
+const char* fold_pass_kernel(FoldPass pass, bool packed_hops);
+
 // early_launch: launch the register passes as programmatic dependents of the
 // kernel before them on the stream (they read only the plan's tables before
 // griddepcontrol.wait, so their prologue overlaps that kernel's tail).

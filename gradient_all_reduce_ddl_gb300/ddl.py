@@ -37,7 +37,7 @@ EXPORTS = [
     "ddl_plan_create", "ddl_plan_set_layers", "ddl_plan_set_mode", "ddl_plan_set_kernel", "ddl_allreduce",
     "ddl_allreduce_bucket", "ddl_allreduce_host", "ddl_overlap_begin", "ddl_bucket_ready", "ddl_overlap_end",
     "ddl_plan_num_buckets", "ddl_plan_bucket_range", "ddl_plan_traffic", "ddl_plan_fold_order",
-    "ddl_plan_launches", "ddl_plan_check", "ddl_status_string", "ddl_plan_destroy", "ddl_allreduce_noalloc",
+    "ddl_plan_launches", "ddl_plan_kernel_name", "ddl_plan_check", "ddl_status_string", "ddl_plan_destroy", "ddl_allreduce_noalloc",
     "ddl_plan_cost", "ddl_plan_set_torus_dims", "ddl_allreduce_sgd", "ddl_selftest_wait_timeout",
     "ddl_allreduce_slab", "ddl_noalloc_check",
 ]
@@ -77,6 +77,7 @@ _sig("ddl_plan_traffic", _i, _vp, _P(_u64), _P(_u64))
 _sig("ddl_plan_cost", _i, _vp, ctypes.c_double, ctypes.c_double, _i, _P(ctypes.c_double))
 _sig("ddl_plan_fold_order", _i, _vp, _sz, _P(ctypes.c_int32), _P(ctypes.c_int32), _P(ctypes.c_int32))
 _sig("ddl_plan_launches", _i, _vp, _P(_u64))
+_sig("ddl_plan_kernel_name", _i, _vp, _P(ctypes.c_char_p))
 _sig("ddl_plan_check", _i, _vp)
 _sig("ddl_selftest_wait_timeout", _i, _vp, ctypes.c_uint32, _vp)
 _sig("ddl_status_string", ctypes.c_char_p, _i)
@@ -223,6 +224,13 @@ def ddl_plan_fold_order(plan, i, P):
     return list(order), inner.value, groups.value
 
 
+def ddl_plan_kernel_name(plan):
+    """The kernel ddl_allreduce launches for the plan with 16-byte-aligned buffers."""
+    name = ctypes.c_char_p()
+    _ok(_lib.ddl_plan_kernel_name(plan, ctypes.byref(name)), "ddl_plan_kernel_name")
+    return name.value.decode()
+
+
 def ddl_plan_launches(plan):
     n = ctypes.c_uint64()
     _ok(_lib.ddl_plan_launches(plan, ctypes.byref(n)), "ddl_plan_launches")
@@ -364,6 +372,11 @@ class Plan:
 
     def fold_order(self, i):
         return ddl_plan_fold_order(self.handle, i, self.P)
+
+    @property
+    def kernel_name(self):
+        """The kernel ddl_allreduce launches (16-byte-aligned buffers)."""
+        return ddl_plan_kernel_name(self.handle)
 
     def cost(self, alpha_s, beta_s_per_byte, links=1):
         """alpha-beta model of this schedule on P real workers with `links`

@@ -340,6 +340,18 @@ ddl_status_t ddl_plan_fold_order(ddl_plan_t plan, size_t i, int32_t* order, int3
 /* Number of kernels this plan has launched since it was created. */
 ddl_status_t ddl_plan_launches(ddl_plan_t plan, uint64_t* n);
 
+/* Introspection: the kernel that ddl_allreduce launches for this plan, in its
+ * current mode and kernel choice, when every rank buffer is 16-byte aligned:
+ * "fold_ldg_kernel" (the register pass), "fold_small_kernel" (small items of
+ * one unrounded fold group), "fold_lat_kernel" or "fold_lat_kernel (one
+ * group)" (small items of P >= 16 ranks staged in shared memory),
+ * "fold_nd_kernel", "fold_nd_h2_kernel" or "fold_lat_nd_kernel" (n-D torus),
+ * "fold_bulk_kernel", "fold_chunked_kernel" (staged choices), or "step_kernel"
+ * (stepwise mode).  *name points to a static string.  Host-only; the one rule
+ * that depends on the device (how many latency-pass CTAs fit at once, for a
+ * single fold group) assumes a GB300's 152 SMs when no device is present. */
+ddl_status_t ddl_plan_kernel_name(ddl_plan_t plan, const char** name);
+
 /* Waits for the plan's device work and reads its kernels' error word:
  * DDL_ERR_DEVICE_CHECK if a kernel found a bad table entry or a bounded wait
  * ran out (the word is then cleared), DDL_OK otherwise. */

@@ -209,6 +209,55 @@ def test_kernel_choice_range(ddl):
             assert ddl._lib.ddl_plan_set_kernel(plan.handle, k) == ddl.DDL_ERR_INVALID_ARG, k
 
 
+# (plan, the kernel ddl_allreduce launches): large buffers take the register
+# pass; small items of P >= 16 ranks the latency pass (one-group instance for a
+# single fold group, until its items exceed one wave of CTAs); small items of
+# one unrounded group below that the small-item pass; the n-D torus its own
+# passes; stepwise mode the step kernel; a staged choice its kernel.
+DISPATCH = [
+    (dict(P=16, N=3_000_000), "fold_ldg_kernel"),
+    (dict(P=16, N=25_557_032, topo="torus", X=4, Y=4), "fold_ldg_kernel"),
+    (dict(P=32, N=25_557_032, dtype="f16", topo="torus", X=8, Y=4), "fold_ldg_kernel"),
+    (dict(P=4, N=65_536), "fold_small_kernel"),
+    (dict(P=8, N=16_384, dtype="f16"), "fold_ldg_kernel"),            # binary16 hops: not unrounded
+    (dict(P=8, N=16_384, dtype="f16", mode="rankorder"), "fold_small_kernel"),
+    (dict(P=8, N=16_384, topo="torus", X=4, Y=2), "fold_ldg_kernel"),
+    (dict(P=16, N=16_384), "fold_lat_kernel (one group)"),
+    (dict(P=16, N=16_384, topo="torus", X=4, Y=4), "fold_lat_kernel"),
+    (dict(P=32, N=16_384, dtype="f16", topo="torus", X=8, Y=4), "fold_lat_kernel"),
+    (dict(P=64, N=16_384, topo="multiring", k=4), "fold_lat_kernel (one group)"),
+    (dict(P=64, N=100_000, topo="multiring", k=4), "fold_small_kernel"),  # past one wave of the latency pass
+    (dict(P=64, N=16_384, topo="torus_nd", dims=[4, 4, 4]), "fold_lat_nd_kernel"),
+    (dict(P=64, N=2_000_000, topo="torus_nd", dims=[4, 4, 4]), "fold_nd_kernel"),
+    (dict(P=32, N=2_000_000, dtype="f16", topo="torus_nd", dims=[4, 4, 2]), "fold_nd_h2_kernel"),
+    (dict(P=16, N=16_384, mode="stepwise"), "step_kernel"),
+    (dict(P=16, N=16_384, kernel="chunked"), "fold_chunked_kernel"),
+    (dict(P=16, N=1_000_000, kernel="bulkload"), "fold_bulk_kernel"),
+]
+
+
+@pytest.mark.parametrize("case,want", DISPATCH, ids=[f"{i}-{w}" for i, (_, w) in enumerate(DISPATCH)])
+def test_dispatch_rules(ddl, case, want):
+    """ddl_plan_kernel_name reports the pass the library's own dispatch takes
+    (the same function the launcher switches on), host-only."""
+    with ddl.Plan(**case) as plan:
+        assert plan.kernel_name == want
+
+
+def test_kernel_name_follows_mode_and_kernel_changes(ddl):
+    with ddl.Plan(16, 16_384, topo="torus", X=4, Y=4) as plan:
+        assert plan.kernel_name == "fold_lat_kernel"
+        plan.set_mode("rankorder")
+        assert plan.kernel_name == "fold_lat_kernel (one group)"
+        plan.set_mode("stepwise")
+        assert plan.kernel_name == "step_kernel"
+        plan.set_mode("fused")
+        plan.set_kernel("chunked")
+        assert plan.kernel_name == "fold_chunked_kernel"
+    with pytest.raises(ddl.DDLError):
+        ddl.ddl_plan_kernel_name(None)
+
+
 def test_layer_sizes_that_would_wrap_are_refused(ddl):
     """A layer list whose sum wraps around 2^64 to N is not a partition of N."""
     with ddl.Plan(3, 1) as plan:
