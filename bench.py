@@ -65,9 +65,9 @@ SECONDARY = ("ring4_int", "torus4x4_resnet50", "torus8x4_resnet50_f16", "multiri
 # algorithmic bytes; a changed kernel source reports null.
 NCU_TRAFFIC = {
     # P = 16 x 20,000,000 fp32 (1.28 GB resident, above L2): 2.56 GB algorithmic per launch
-    ("ring", "f32", "ldg", "e1b2ea7f1275826b"): (1_280_196_096 + 1_220_354_048, 2_560_000_000),
-    ("multiring", "f32", "ldg", "e1b2ea7f1275826b"): (1_280_230_912 + 1_220_017_408, 2_560_000_000),
-    ("torus", "f32", "ldg", "e1b2ea7f1275826b"): (1_280_195_584 + 1_220_519_680, 2_560_000_000),
+    ("ring", "f32", "ldg", "fc10bd0ebfe172e4"): (1_280_207_104 + 1_220_646_144, 2_560_000_000),
+    ("multiring", "f32", "ldg", "fc10bd0ebfe172e4"): (1_280_201_216 + 1_220_586_240, 2_560_000_000),
+    ("torus", "f32", "ldg", "fc10bd0ebfe172e4"): (1_280_230_912 + 1_220_674_816, 2_560_000_000),
 }
 
 KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]

@@ -1583,19 +1583,28 @@ FoldPass fold_pass(const FoldParams& p, uint32_t n_items, bool f16, int variant)
     return variant == kVarLdg && lat_nd_applies(p) ? kPassNdLatency : kPassNdRegister;
   if (variant == kVarBulkLoad) return kPassBulkLoad;
   if (variant == kVarChunked) return kPassChunked;
-  // small items of many ranks: the latency pass -- except for a single
-  // unrounded group whose items need more than one wave of it, where the
-  // small-item pass's occupancy wins (P = 64 multi-ring, 3 latency CTAs per SM
-  // with 1 KB items: 409 items 16.6 against 18.4 us per all-reduce, 646 items
-  // 26.0 against 20.5 us)
+  // small items of many ranks: the latency pass, within the limits where it
+  // measured fastest (per all-reduce in graph replay):
+  // - several fold groups: items of at most 2 KB per rank; with 4 KB items two
+  //   of its CTAs fit on an SM and the register pass wins (4x4 torus at
+  //   524,288 elements: 16.6 against 10.0 us; 8x4 fp16 torus at 524,288, 2 KB
+  //   items: 18.0 against 18.9 us);
+  // - a single unrounded group: items within one wave of its CTAs, else the
+  //   small-item pass's occupancy wins (P = 64 multi-ring, 3 latency CTAs per
+  //   SM with 1 KB items: 409 items 16.6 against 18.4 us, 646 items 26.0
+  //   against 20.5 us); and below 32 ranks items of at most 512 bytes, where
+  //   the small-item pass's chain of P / 4 round trips is short (P = 16 ring
+  //   at 262,144 elements, 2 KB items: 7.05 against 5.74 us).
   const bool unrounded = !f16 || !p.round_hops;
   const bool single = unrounded && p.groups == 1 && p.inner == p.P;
   const bool small_items = p.tile_bytes <= (uint32_t)kThreads * 16u;
   if (p.vector_ok && small_items && p.P >= kLatMinP && p.groups >= 1 && p.inner >= 1 &&
       (int64_t)p.inner * p.groups == p.P) {
     const uint32_t smem = lat_smem_of(p, f16);
-    if (smem <= kLatMaxSmem && (!single || n_items <= lat_wave(smem)))
-      return p.groups == 1 ? kPassLatencySingle : kPassLatency;
+    bool take = smem <= kLatMaxSmem;
+    if (p.groups > 1) take = take && p.tile_bytes <= 2048u;
+    if (single) take = take && n_items <= lat_wave(smem) && (p.P >= 32 || p.tile_bytes <= 512u);
+    if (take) return p.groups == 1 ? kPassLatencySingle : kPassLatency;
   }
   // small items of a single unrounded group: the small-item pass (one column
   // per thread covers up to kThreads * 16 bytes per rank)
