@@ -227,7 +227,8 @@ __device__ __forceinline__ bool load_item(const FoldParams& p, char** s_ptr, Ite
 
 // ---------------------------------------------------------------------------
 // The register pass.  V columns per thread, B ranks' loads in flight,
-// sized for MINB CTAs per SM.  V * kThreads columns cover the largest item.
+// sized for MINB CTAs per SM.  V * kThreads columns must cover the largest
+// item (V * 4 KB per rank); the launcher picks V from the plan's item size.
 // ---------------------------------------------------------------------------
 #ifndef DDL_LDG_F32_B
 #define DDL_LDG_F32_B 8
@@ -244,7 +245,6 @@ __device__ __forceinline__ bool load_item(const FoldParams& p, char** s_ptr, Ite
 template <bool F16, bool H2, int V, int B, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB) fold_ldg_kernel(const __grid_constant__ FoldParams p) {
   static_assert(F16 || !H2, "packed hops are binary16 only");
-  static_assert(V * kThreads * 16 >= kTileBytes, "an item must fit one pass of the columns");
   constexpr int L = F16 ? 8 : 4;  // elements per 16-byte column
   __shared__ char* s_ptr[kMaxP];
   Item s_item;
@@ -1544,6 +1544,20 @@ cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t strea
   // is refused (the element-wise path, taken for unaligned buffers, covers
   // any item)
   if (p.vector_ok && p.tile_bytes > (uint32_t)kTileBytes) return cudaErrorInvalidValue;
+  // 4 KB items (buffers of 1.2 to 2.5 MB per rank, L2-resident): one column
+  // per thread keeps every thread busy, and the smaller register set fits
+  // three CTAs per SM (four with packed binary16 hops).  Per all-reduce in
+  // graph replay: 4x4 torus at 524,288 elements 10.07 against 8.86 us, 8x4
+  // fp16 torus at 1,048,576 elements 23.78 against 19.04 us.  With 1 KB items
+  // it measured slower (P = 8 torus at 65,536 elements 2.46 against 3.08 us).
+  if (p.tile_bytes == (uint32_t)kThreads * 16u) {
+    if constexpr (F16) {
+      if (p.round_hops) return launch_items(fold_ldg_kernel<true, true, 1, 8, 4>, p, n_items, stream, early);
+      return launch_items(fold_ldg_kernel<true, false, 1, 8, 3>, p, n_items, stream, early);
+    } else {
+      return launch_items(fold_ldg_kernel<false, false, 1, 8, 3>, p, n_items, stream, early);
+    }
+  }
   if constexpr (F16) {
     if (p.round_hops)
       return launch_items(fold_ldg_kernel<true, true, 2, DDL_LDG_F16_B, DDL_LDG_MINB>, p, n_items, stream, early);
@@ -1557,6 +1571,18 @@ cudaError_t launch_ldg(const FoldParams& p, uint32_t n_items, cudaStream_t strea
 // up to 8 KB); fp16 with rounded hops folds packed pairs, fp16 without them
 // (unused by the plans) one column (4 KB).
 cudaError_t launch_nd(const FoldParams& p, uint32_t n_items, bool f16, cudaStream_t stream, bool early) {
+  // 2 and 4 KB items: one column per thread, as in the 2-level pass (4x4x4
+  // torus at 262,144 elements 34.1 against 27.0 us, 4x4x2 fp16 torus at
+  // 1,048,576 elements 24.0 against 19.4 us per all-reduce in graph replay)
+  if (p.tile_bytes >= 2048u && p.tile_bytes <= (uint32_t)kThreads * 16u) {
+    if (f16 && p.round_hops) {
+      if (p.nlev < 1 || p.nlev > 4) return cudaErrorInvalidValue;
+      void (*const h1[4])(FoldParams) = {fold_nd_h2_kernel<1, DDL_ND_H2_B1, 1>, fold_nd_h2_kernel<1, DDL_ND_H2_B1, 2>,
+                                         fold_nd_h2_kernel<1, DDL_ND_H2_B3, 3>, fold_nd_h2_kernel<1, DDL_ND_H2_B4, 4>};
+      return launch_items(h1[p.nlev - 1], p, n_items, stream, early);
+    }
+    return launch_items(f16 ? fold_nd_kernel<true, 1, 8> : fold_nd_kernel<false, 1, 8>, p, n_items, stream, early);
+  }
   if (f16 && p.round_hops) {
     if (p.nlev < 1 || p.nlev > 4) return cudaErrorInvalidValue;
     void (*const h2[4])(FoldParams) = {fold_nd_h2_kernel<2, DDL_ND_H2_B1, 1>, fold_nd_h2_kernel<2, DDL_ND_H2_B1, 2>,
