@@ -1611,9 +1611,10 @@ FoldPass fold_pass(const FoldParams& p, uint32_t n_items, bool f16, int variant)
   if (variant == kVarChunked) return kPassChunked;
   // small items of many ranks: the latency pass, within the limits where it
   // measured fastest (per all-reduce in graph replay):
-  // - several fold groups: items of at most 2 KB per rank; with 4 KB items two
-  //   of its CTAs fit on an SM and the register pass wins (4x4 torus at
-  //   524,288 elements: 16.6 against 10.0 us; 8x4 fp16 torus at 524,288, 2 KB
+  // - several fold groups, or binary16 hops: items of at most 2 KB per rank;
+  //   with 4 KB items two of its CTAs fit on an SM and the register pass wins
+  //   (4x4 torus at 524,288 elements: 16.6 against 10.0 us; P = 16 fp16 ring
+  //   at 1,048,576: 16.9 against 10.0 us; 8x4 fp16 torus at 524,288, 2 KB
   //   items: 18.0 against 18.9 us);
   // - a single unrounded group: items within one wave of its CTAs, else the
   //   small-item pass's occupancy wins (P = 64 multi-ring, 3 latency CTAs per
@@ -1628,7 +1629,7 @@ FoldPass fold_pass(const FoldParams& p, uint32_t n_items, bool f16, int variant)
       (int64_t)p.inner * p.groups == p.P) {
     const uint32_t smem = lat_smem_of(p, f16);
     bool take = smem <= kLatMaxSmem;
-    if (p.groups > 1) take = take && p.tile_bytes <= 2048u;
+    if (!single) take = take && p.tile_bytes <= 2048u;
     if (single) take = take && n_items <= lat_wave(smem) && (p.P >= 32 || p.tile_bytes <= 512u);
     if (take) return p.groups == 1 ? kPassLatencySingle : kPassLatency;
   }

@@ -232,6 +232,8 @@ DISPATCH = [
     (dict(P=16, N=262_144, topo="torus", X=4, Y=4), "fold_lat_kernel"),  # 2 KB items, four groups
     (dict(P=16, N=524_288, topo="torus", X=4, Y=4), "fold_ldg_kernel"),  # 4 KB items
     (dict(P=32, N=524_288, dtype="f16", topo="torus", X=8, Y=4), "fold_lat_kernel"),
+    (dict(P=16, N=524_288, dtype="f16"), "fold_lat_kernel (one group)"),  # binary16 hops, 2 KB items
+    (dict(P=16, N=1_048_576, dtype="f16"), "fold_ldg_kernel"),            # binary16 hops, 4 KB items
     (dict(P=64, N=16_384, topo="torus_nd", dims=[4, 4, 4]), "fold_lat_nd_kernel"),
     (dict(P=64, N=2_000_000, topo="torus_nd", dims=[4, 4, 4]), "fold_nd_kernel"),
     (dict(P=32, N=2_000_000, dtype="f16", topo="torus_nd", dims=[4, 4, 2]), "fold_nd_h2_kernel"),
