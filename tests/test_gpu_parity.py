@@ -244,6 +244,35 @@ def test_small_buffer_passes_match_oracle(ddl, case, dtype, mode):
         assert np.array_equal(to_numpy_bits(bufs[r]), got0), r
 
 
+# Buffers between the latency passes and the HBM regime, each landing on the
+# pass named (2 and 4 KB work items: the one-column register passes, the
+# small-item pass with 4 KB items, the latency pass at its 2 KB limit), several
+# with sizes whose chunks end inside 16-byte columns.
+MID_SIZE = [
+    (dict(P=16, N=524_288, topo="torus", X=4, Y=4), "fold_ldg_kernel"),
+    (dict(P=16, N=600_001, topo="torus", X=4, Y=4), "fold_ldg_kernel"),
+    (dict(P=8, N=400_003, topo="torus", X=4, Y=2), "fold_ldg_kernel"),
+    (dict(P=32, N=1_048_576, dtype="f16", topo="torus", X=8, Y=4), "fold_ldg_kernel"),
+    (dict(P=16, N=1_000_003, dtype="f16"), "fold_ldg_kernel"),
+    (dict(P=16, N=524_288, dtype="f16"), "fold_lat_kernel (one group)"),
+    (dict(P=16, N=262_144, topo="torus", X=4, Y=4), "fold_lat_kernel"),
+    (dict(P=16, N=500_001), "fold_small_kernel"),
+    (dict(P=64, N=262_144, topo="torus_nd", dims=[4, 4, 4]), "fold_nd_kernel"),
+    (dict(P=64, N=500_003, topo="torus_nd", dims=[4, 4, 4]), "fold_nd_kernel"),
+    (dict(P=32, N=1_048_576, dtype="f16", topo="torus_nd", dims=[4, 4, 2]), "fold_nd_h2_kernel"),
+    (dict(P=32, N=333_333, dtype="f16", topo="torus_nd", dims=[4, 4, 2]), "fold_lat_nd_kernel"),
+    (dict(P=64, N=400_001, dtype="f16", topo="torus_nd", dims=[4, 4, 4]), "fold_nd_h2_kernel"),
+]
+
+
+@pytest.mark.parametrize("case,kernel", MID_SIZE, ids=[f"{i}-{k}" for i, (_, k) in enumerate(MID_SIZE)])
+def test_mid_size_passes_match_oracle(ddl, case, kernel):
+    w = _w(seed=29, **case)
+    with ddl.Plan.for_workload(w) as plan:
+        assert plan.kernel_name == kernel
+    _check_exact(ddl, w)
+
+
 @pytest.mark.parametrize("kernel", ["bulkload", "chunked"])
 @pytest.mark.parametrize("P", [2, 4])
 def test_small_p_with_a_staged_kernel_choice(ddl, kernel, P):
