@@ -92,8 +92,11 @@ typedef enum {
 } ddl_mode_t;
 
 typedef enum {
-  DDL_KERNEL_AUTO = 0,  /* the library's choice */
-  DDL_KERNEL_LDG = 1,   /* fused pass with 16-byte register loads and stores */
+  DDL_KERNEL_AUTO = 0,  /* the library's choice (the same as DDL_KERNEL_LDG for ddl_allreduce;
+                           see ddl_allreduce_host and the bucket scheduler for the others) */
+  DDL_KERNEL_LDG = 1,   /* the column passes with 16-byte loads and stores: the register pass,
+                           and for small buffers the small-item and shared-memory latency passes
+                           (ddl_plan_kernel_name reports which one a plan takes) */
   /* 2 is not used (a staged pass with bulk stores, removed: it was slower
      than the register pass at every P measured) */
   DDL_KERNEL_BULK_LOAD = 3, /* bulk async loads of all ranks' tiles into shared memory, stores
