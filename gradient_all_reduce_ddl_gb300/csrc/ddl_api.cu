@@ -521,6 +521,7 @@ ddl_status_t ddl_allreduce_sgd(ddl_plan_t p, void* const* grad_bufs, float* cons
   sp.vector_ok = (aligned && p->checked_sgd_aligned) ? 1 : 0;
   sp.keep_grads = keep_grads ? 1 : 0;
   sp.has_mom = mom_bufs ? 1 : 0;
+  sp.tile_bytes = p->spec.tile_bytes;
   for (int r = 0; r < P; ++r) {
     sp.grads[r] = grad_bufs[r];
     sp.params[r] = param_bufs[r];

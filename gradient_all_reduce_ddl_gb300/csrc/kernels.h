@@ -59,6 +59,7 @@ struct SgdParams {
   int32_t vector_ok;   // every buffer 16-byte aligned
   int32_t keep_grads;  // store the all-reduced gradient back
   int32_t has_mom;     // momentum buffers given (else v = d)
+  uint32_t tile_bytes; // gradient bytes per rank of the largest item
   void* grads[kMaxPSgd];
   float* params[kMaxPSgd];
   float* moms[kMaxPSgd];

@@ -13,6 +13,8 @@
 // again for the update.
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "kernels.h"
 
 namespace ddl {
@@ -279,18 +281,228 @@ __global__ void __launch_bounds__(kThreads, 2) fold_sgd_kernel(const __grid_cons
   }
 }
 
+// ---------------------------------------------------------------------------
+// The staged pass for small items.  With a small buffer the register pass
+// above is a chain of dependent round trips per CTA: the fold's batches of
+// ranks, then the update's parameter and momentum loads, rank after rank.
+// Here the CTA loads every rank's gradient tile, parameter and momentum
+// columns of its item into shared memory at once (one round trip, all threads
+// issuing loads), folds each row group of the schedule (a thread per group and
+// column), folds the group totals (a thread per column) -- or, for a single
+// group, takes its fold as the result -- and then updates every rank's
+// parameters and momenta from shared memory, all threads at once.  The adds,
+// their order and roundings, the scale, the storage rounding of the gradient
+// and the update (sgd_one) are those of the register pass.
+// Shared memory: P x tile gradient bytes, P x tile x (4 / esize) parameter and
+// as many momentum bytes, the group totals and the result in binary32 as
+// 16-byte slices (row g * Q + q, a column per 16 bytes), the result in storage
+// form (16 bytes per column).
+// ---------------------------------------------------------------------------
+__host__ __device__ constexpr uint32_t sgd_lat_smem_bytes(uint32_t P, uint32_t groups, uint32_t tile, uint32_t q) {
+  return P * tile + 2u * P * tile * q + groups * tile * q + tile * q + tile;
+}
+
+template <bool F16, bool SINGLE>
+__global__ void __launch_bounds__(kThreads) fold_sgd_lat_kernel(const __grid_constant__ SgdParams p) {
+  constexpr int L = F16 ? 8 : 4;  // gradient elements per 16-byte column
+  constexpr int Q = L / 4;        // 16-byte binary32 vectors per column of parameters
+  extern __shared__ __align__(16) unsigned char s_sgd[];
+  __shared__ char* s_g[kMaxPSgd];
+  __shared__ float* s_p[kMaxPSgd];
+  __shared__ float* s_m[kMaxPSgd];
+  asm volatile("griddepcontrol.launch_dependents;");
+  const Item s_item = p.items[p.item0 + blockIdx.x];
+  const uint64_t off = (uint64_t)s_item.seg * (uint64_t)p.P;
+  if (!(s_item.seg < p.n_segs && off + (uint64_t)p.P <= p.n_orders)) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrBadItem);
+    return;
+  }
+  for (int t = threadIdx.x; t < p.P; t += kThreads) {
+    unsigned r = p.orders[off + t];
+    r = r < (unsigned)p.P ? r : 0;
+    s_g[t] = static_cast<char*>(p.grads[r]);
+    s_p[t] = p.params[r];
+    s_m[t] = p.moms[r];
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  const int P = p.P, inner = p.inner, groups = p.groups;
+  const bool rh = F16 && p.round_hops;
+  const uint32_t T = p.tile_bytes, CT = T / 16u;
+  const uint64_t eb = s_item.begin, ee = eb + s_item.len;
+  const uint64_t vb = (eb + L - 1) / L, ve = ee / L;
+  if (!p.vector_ok || vb >= ve) {
+    for (uint64_t e = eb + threadIdx.x; e < ee; e += kThreads) sgd_scalar<F16>(p, s_g, s_p, s_m, e, inner, groups, rh);
+    return;
+  }
+  const uint32_t ncols = (uint32_t)(ve - vb);  // <= T / 16
+  unsigned char* s_grad = s_sgd;
+  float4* s_par = reinterpret_cast<float4*>(s_sgd + (size_t)P * T);
+  float4* s_mom = s_par + (size_t)P * CT * Q;
+  float4* s_tot = s_mom + (size_t)P * CT * Q;
+  float4* s_res = s_tot + (size_t)groups * CT * Q;
+  uint4* s_st = reinterpret_cast<uint4*>(s_res + (size_t)CT * Q);
+
+  // every rank's gradient column, parameters and momenta, all loads in flight
+  for (uint32_t i = threadIdx.x; i < (uint32_t)P * ncols; i += kThreads) {
+    const uint32_t t = i / ncols, c = i % ncols;
+    *reinterpret_cast<uint4*>(s_grad + (size_t)t * T + c * 16u) =
+        __ldcs(reinterpret_cast<const uint4*>(s_g[t]) + vb + c);
+    const float4* pv = reinterpret_cast<const float4*>(s_p[t]) + (vb + c) * Q;
+    const float4* mv = reinterpret_cast<const float4*>(s_m[t]) + (vb + c) * Q;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      s_par[((size_t)t * CT + c) * Q + q] = __ldcs(pv + q);
+      if (p.has_mom) s_mom[((size_t)t * CT + c) * Q + q] = __ldcs(mv + q);
+    }
+  }
+  __syncthreads();
+
+  // each row group of each column: the left fold of its inner positions
+  for (uint32_t i = threadIdx.x; i < (uint32_t)groups * ncols; i += kThreads) {
+    const int g = (int)(i / ncols);
+    const uint32_t c = i % ncols;
+    float a[L];
+    for (int h = 0; h < inner; ++h) {
+      const int t = g * inner + h;
+      float f[L];
+      unpack<F16>(*reinterpret_cast<const uint4*>(s_grad + (size_t)t * T + c * 16u), f);
+      if (h == 0) {
+#pragma unroll
+        for (int l = 0; l < L; ++l) a[l] = f[l];
+      } else {
+        const bool round = rh && !(t == P - 1 && groups == 1);  // the final add of one group is not
+#pragma unroll
+        for (int l = 0; l < L; ++l) {
+          const float v = __fadd_rn(a[l], f[l]);
+          a[l] = round ? round_h(v) : v;
+        }
+      }
+    }
+    if constexpr (SINGLE) {  // one group: its fold, scaled, is the gradient
+#pragma unroll
+      for (int l = 0; l < L; ++l) a[l] = __fmul_rn(a[l], p.scale);
+      const uint4 st = pack<F16>(a);
+      if (F16) unpack<F16>(st, a);  // the update reads the gradient as stored
+      s_st[c] = st;
+#pragma unroll
+      for (int q = 0; q < Q; ++q) s_res[(size_t)q * CT + c] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < Q; ++q)
+        s_tot[((size_t)g * Q + q) * CT + c] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+    }
+  }
+  __syncthreads();
+
+  if constexpr (!SINGLE) {  // each column: the left fold of its group totals
+    for (uint32_t c = threadIdx.x; c < ncols; c += kThreads) {
+      float o[L];
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        const float4 v = s_tot[(size_t)q * CT + c];
+        o[4 * q] = v.x, o[4 * q + 1] = v.y, o[4 * q + 2] = v.z, o[4 * q + 3] = v.w;
+      }
+      for (int g = 1; g < groups; ++g) {
+        const bool round = rh && g != groups - 1;  // the last group's add is the final one
+        float t4[L];
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+          const float4 v = s_tot[((size_t)g * Q + q) * CT + c];
+          t4[4 * q] = v.x, t4[4 * q + 1] = v.y, t4[4 * q + 2] = v.z, t4[4 * q + 3] = v.w;
+        }
+#pragma unroll
+        for (int l = 0; l < L; ++l) {
+          const float v = __fadd_rn(o[l], t4[l]);
+          o[l] = round ? round_h(v) : v;
+        }
+      }
+#pragma unroll
+      for (int l = 0; l < L; ++l) o[l] = __fmul_rn(o[l], p.scale);
+      const uint4 st = pack<F16>(o);
+      if (F16) unpack<F16>(st, o);
+      s_st[c] = st;
+#pragma unroll
+      for (int q = 0; q < Q; ++q) s_res[(size_t)q * CT + c] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    }
+    __syncthreads();
+  }
+
+  // the update of every rank's parameters and momenta, and the gradient stores
+  for (uint32_t i = threadIdx.x; i < (uint32_t)P * ncols * Q; i += kThreads) {
+    const uint32_t t = i / (ncols * Q), r = i % (ncols * Q), c = r / Q, q = r % Q;
+    const float4 g4 = s_res[(size_t)q * CT + c];
+    float4 pw = s_par[((size_t)t * CT + c) * Q + q];
+    float4 mw = p.has_mom ? s_mom[((size_t)t * CT + c) * Q + q] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+    float* pe = reinterpret_cast<float*>(&pw);
+    float* me = reinterpret_cast<float*>(&mw);
+#pragma unroll
+    for (int l = 0; l < 4; ++l) pe[l] = sgd_one(gv[l], pe[l], &me[l], p);
+    __stcs(reinterpret_cast<float4*>(s_p[t]) + (vb + c) * Q + q, pw);
+    if (p.has_mom) __stcs(reinterpret_cast<float4*>(s_m[t]) + (vb + c) * Q + q, mw);
+    if (p.keep_grads && q == 0) __stcs(reinterpret_cast<uint4*>(s_g[t]) + vb + c, s_st[c]);
+  }
+  const uint64_t nh = vb * L - eb, nt = ee - ve * L;
+  if (threadIdx.x < nh + nt) {
+    const uint64_t e = threadIdx.x < nh ? eb + threadIdx.x : ve * L + (threadIdx.x - nh);
+    sgd_scalar<F16>(p, s_g, s_p, s_m, e, inner, groups, rh);
+  }
+}
+
+#ifndef DDL_SGD_LAT_MAX_TILE
+#define DDL_SGD_LAT_MAX_TILE 1024
+#endif
+constexpr uint32_t kSgdLatMaxSmem = 96u * 1024u;
+
+// The opt-in above 48 KB of shared memory, once per kernel and device.
+cudaError_t sgd_smem_opt_in(void (*kernel)(SgdParams), std::atomic<bool>* ready) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!ready[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSgdLatMaxSmem);
+    if (e != cudaSuccess) return e;
+    ready[dev].store(true, std::memory_order_release);
+  }
+  return cudaSuccess;
+}
+
 }  // namespace
 
 // One CTA per work item, launched as a programmatic dependent of the kernel
 // before it on the stream: its table prologue overlaps that kernel's tail.
+// Small items (up to DDL_SGD_LAT_MAX_TILE bytes per rank) whose ranks'
+// gradients, parameters and momenta fit in 96 KB of shared memory take the
+// staged pass.
 cudaError_t launch_sgd(const SgdParams& p, uint32_t n_items, bool f16, cudaStream_t stream) {
   if (n_items == 0) return cudaSuccess;
-  void (*kernel)(SgdParams) = f16 && p.round_hops ? fold_sgd_kernel<true, true>
-                              : f16               ? fold_sgd_kernel<true, false>
-                                                  : fold_sgd_kernel<false, false>;
+  uint32_t smem = 0;
+  void (*kernel)(SgdParams) = nullptr;
+  if (p.vector_ok && p.tile_bytes <= (uint32_t)DDL_SGD_LAT_MAX_TILE && p.tile_bytes % 16u == 0 && p.groups >= 1 &&
+      p.inner >= 1 && (int64_t)p.inner * p.groups == p.P) {
+    smem = sgd_lat_smem_bytes((uint32_t)p.P, (uint32_t)p.groups, p.tile_bytes, f16 ? 2u : 1u);
+    if (smem <= kSgdLatMaxSmem) {
+      static std::atomic<bool> ready[2][2][64];
+      const bool single = p.groups == 1;
+      kernel = f16 ? (single ? fold_sgd_lat_kernel<true, true> : fold_sgd_lat_kernel<true, false>)
+                   : (single ? fold_sgd_lat_kernel<false, true> : fold_sgd_lat_kernel<false, false>);
+      const cudaError_t e = sgd_smem_opt_in(kernel, ready[f16 ? 1 : 0][single ? 1 : 0]);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  if (!kernel) {
+    smem = 0;
+    kernel = f16 && p.round_hops ? fold_sgd_kernel<true, true>
+             : f16               ? fold_sgd_kernel<true, false>
+                                 : fold_sgd_kernel<false, false>;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_items);
   cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

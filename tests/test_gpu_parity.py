@@ -155,6 +155,12 @@ SGD_CASES = [
     dict(P=16, N=99_999, topo="torus", X=4, Y=4),
     dict(P=32, N=20_000, topo="torus", X=8, Y=4, dtype="f16"),
     dict(P=8, N=30_011, dtype="f16", bucket_bytes=20_000),
+    # small items: the staged pass (one group; several groups with binary16
+    # hops and cut columns; P < 16), and 2 KB items in the register pass
+    dict(P=64, N=9_001, topo="multiring", k=4),
+    dict(P=32, N=16_385, topo="torus", X=8, Y=4, dtype="f16"),
+    dict(P=8, N=20_001, topo="torus", X=4, Y=2, dtype="f16"),
+    dict(P=16, N=200_003, topo="torus", X=4, Y=4),
 ]
 
 
