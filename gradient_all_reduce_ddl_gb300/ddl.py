@@ -289,6 +289,7 @@ class Plan:
         self.P, self.N, self.dtype = int(P), int(N), dtype
         self._last_ptrs, self._last_arr = None, None
         self._last_stream, self._last_handle = _NO_STREAM, None
+        self._sgd_key, self._sgd_arrs = None, None
         topo_t = ddl_topology_t(TOPOLOGIES[topo], int(k), int(X), int(Y))
         self.handle = ddl_plan_create(self.P, self.N, DTYPES[dtype], topo_t, int(bucket_bytes))
         try:
@@ -330,8 +331,19 @@ class Plan:
 
     def allreduce_sgd(self, grad_bufs, param_bufs, mom_bufs, scale, lr, momentum=0.0, weight_decay=0.0,
                       keep_grads=True, stream=None):
-        ddl_allreduce_sgd(self.handle, grad_bufs, param_bufs, mom_bufs, scale, lr, momentum, weight_decay,
-                          keep_grads, stream)
+        # as in allreduce: the three pointer arrays are rebuilt only when a
+        # buffer changes (the pointers are compared on every call)
+        try:
+            key = ([b.data_ptr() for b in grad_bufs], [b.data_ptr() for b in param_bufs],
+                   None if mom_bufs is None else [b.data_ptr() for b in mom_bufs])
+        except AttributeError:
+            key = (_dev_ptrs(grad_bufs), _dev_ptrs(param_bufs), None if mom_bufs is None else _dev_ptrs(mom_bufs))
+        if key != self._sgd_key:
+            self._sgd_key = key
+            self._sgd_arrs = (_ptr_array(key[0]), _ptr_array(key[1]), None if key[2] is None else _ptr_array(key[2]))
+        g, pa, m = self._sgd_arrs
+        _ok(_lib.ddl_allreduce_sgd(self.handle, g, pa, m, scale, lr, momentum, weight_decay, 1 if keep_grads else 0,
+                                   _stream_handle(stream)), "ddl_allreduce_sgd")
 
     def allreduce_slab(self, base, rank_stride_bytes, scale, stream=None):
         ddl_allreduce_slab(self.handle, base, rank_stride_bytes, scale, stream)
