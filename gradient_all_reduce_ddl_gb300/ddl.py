@@ -311,7 +311,7 @@ class Plan:
         return cls(w.P, w.N, w.dtype, w.topo, k=w.k, X=w.X, Y=w.Y, bucket_bytes=w.bucket_bytes,
                    layers=w.layers, dims=getattr(w, "dims", None), **kw)
 
-    def allreduce(self, rank_bufs, scale, stream=None):
+    def _rank_array(self, rank_bufs, stream):
         # the per-call path of small all-reduces: the ctypes pointer array is
         # rebuilt only when the buffers change, and the stream handle is kept
         # for the stream object last seen
@@ -325,7 +325,11 @@ class Plan:
             self._last_stream, self._last_handle = stream, _stream_handle(stream)
             if stream is None:
                 self._last_stream = _NO_STREAM
-        status = _ddl_allreduce(self.handle, self._last_arr, scale, self._last_handle)
+        return self._last_arr, self._last_handle
+
+    def allreduce(self, rank_bufs, scale, stream=None):
+        arr, handle = self._rank_array(rank_bufs, stream)
+        status = _ddl_allreduce(self.handle, arr, scale, handle)
         if status:
             raise DDLError(status, "ddl_allreduce")
 
@@ -349,7 +353,8 @@ class Plan:
         ddl_allreduce_slab(self.handle, base, rank_stride_bytes, scale, stream)
 
     def allreduce_bucket(self, bucket, rank_bufs, scale, stream=None):
-        ddl_allreduce_bucket(self.handle, bucket, rank_bufs, scale, stream)
+        arr, handle = self._rank_array(rank_bufs, stream)
+        _ok(_lib.ddl_allreduce_bucket(self.handle, bucket, arr, scale, handle), "ddl_allreduce_bucket")
 
     def allreduce_host(self, host_bufs, dev_bufs, scale, stream=None):
         ddl_allreduce_host(self.handle, host_bufs, dev_bufs, scale, stream)
