@@ -1112,6 +1112,49 @@ def test_allreduce_captured_in_cuda_graph(ddl):
                 assert np.array_equal(to_numpy_bits(bufs[r]), ref[r]), r
 
 
+@pytest.mark.parametrize("case", [dict(P=32, N=16_385, topo="torus", X=8, Y=4, dtype="f16"),
+                                  dict(P=16, N=300_001, topo="torus", X=4, Y=4)],
+                         ids=["staged-f16", "register-f32"])
+def test_allreduce_sgd_captured_in_cuda_graph(ddl, case):
+    """The fused all-reduce + momentum SGD captured in a CUDA graph (after a
+    first call outside the capture): three replays equal three updates of the
+    oracle, each on the gradients the buffers hold at that replay."""
+    w = _w(seed=53, **case)
+    host = _host_inputs(w)
+    rng = np.random.default_rng(9)
+    p0 = rng.standard_normal(w.N).astype(np.float32)
+    v0 = (rng.standard_normal(w.N) * 0.1).astype(np.float32)
+    lr, mu, wd = 0.05, 0.9, 1e-4
+    p_ref = [p0.copy() for _ in range(w.P)]
+    m_ref = [v0.copy() for _ in range(w.P)]
+    grads = device_bufs_from_host(host, DEV)
+    src = [g.clone() for g in grads]
+    params = [torch.from_numpy(p0).to(DEV) for _ in range(w.P)]
+    moms = [torch.from_numpy(v0).to(DEV) for _ in range(w.P)]
+    with ddl.Plan.for_workload(w) as plan:
+        g_ref = [h.copy() for h in host]
+        oracle.sgd(oracle_cfg(w), g_ref, p_ref, m_ref, w.scale, lr, mu, wd)
+        plan.allreduce_sgd(grads, params, moms, w.scale, lr, mu, wd)   # uploads, outside the capture
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            plan.allreduce_sgd(grads, params, moms, w.scale, lr, mu, wd, stream=s)
+        for _ in range(3):
+            for b, x in zip(grads, src):
+                b.copy_(x)
+            g_ref = [h.copy() for h in host]
+            oracle.sgd(oracle_cfg(w), g_ref, p_ref, m_ref, w.scale, lr, mu, wd)
+            graph.replay()
+            torch.cuda.synchronize()
+        plan.check()
+    for r in range(w.P):
+        assert np.array_equal(params[r].cpu().numpy(), p_ref[r]), ("params", r)
+        assert np.array_equal(moms[r].cpu().numpy(), m_ref[r]), ("moms", r)
+        assert np.array_equal(to_numpy_bits(grads[r]), g_ref[r]), ("grads", r)
+
+
 def test_bounded_wait_timeout_is_reported_and_context_survives(ddl):
     """A wait that runs out (an mbarrier nothing arrives at, 50 ms limit)
     sets the error word; ddl_plan_check reports DDL_ERR_DEVICE_CHECK once,
