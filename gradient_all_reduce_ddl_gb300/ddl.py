@@ -37,8 +37,8 @@ EXPORTS = [
     "ddl_plan_create", "ddl_plan_set_layers", "ddl_plan_set_mode", "ddl_plan_set_kernel", "ddl_allreduce",
     "ddl_allreduce_bucket", "ddl_allreduce_host", "ddl_overlap_begin", "ddl_bucket_ready", "ddl_overlap_end",
     "ddl_plan_num_buckets", "ddl_plan_bucket_range", "ddl_plan_traffic", "ddl_plan_fold_order",
-    "ddl_plan_launches", "ddl_plan_kernel_name", "ddl_plan_check", "ddl_status_string", "ddl_plan_destroy", "ddl_allreduce_noalloc",
-    "ddl_plan_cost", "ddl_plan_set_torus_dims", "ddl_allreduce_sgd", "ddl_selftest_wait_timeout",
+    "ddl_plan_launches", "ddl_plan_kernel_name", "ddl_plan_check", "ddl_status_string", "ddl_plan_destroy",
+    "ddl_allreduce_noalloc", "ddl_plan_cost", "ddl_plan_set_torus_dims", "ddl_allreduce_sgd", "ddl_selftest_wait_timeout",
     "ddl_allreduce_slab", "ddl_noalloc_check",
 ]
 
@@ -271,7 +271,10 @@ def ddl_noalloc_check(stream=None):
 
 # -- convenience object --------------------------------------------------------
 
-_ddl_allreduce = _lib.ddl_allreduce
+# the per-call path of Plan.allreduce: the same entry point without argtypes,
+# given ready-made ctypes arguments (no conversion on each call)
+_ddl_allreduce = ctypes.CDLL(LIB_PATH).ddl_allreduce
+_ddl_allreduce.restype = ctypes.c_int
 _NO_STREAM = object()  # no stream object seen yet (None means the current stream, looked up each call)
 
 TOPOLOGIES = {"ring": DDL_RING, "multiring": DDL_MULTIRING, "torus": DDL_TORUS, "torus_nd": DDL_RING}
@@ -290,8 +293,10 @@ class Plan:
         self._last_ptrs, self._last_arr = None, None
         self._last_stream, self._last_handle = _NO_STREAM, None
         self._sgd_key, self._sgd_arrs = None, None
+        self._scale, self._c_scale = None, None
         topo_t = ddl_topology_t(TOPOLOGIES[topo], int(k), int(X), int(Y))
         self.handle = ddl_plan_create(self.P, self.N, DTYPES[dtype], topo_t, int(bucket_bytes))
+        self._c_handle = self.handle  # a ctypes.c_void_p
         try:
             if layers is not None:
                 ddl_plan_set_layers(self.handle, list(layers))
@@ -304,6 +309,7 @@ class Plan:
         except Exception:
             ddl_plan_destroy(self.handle)
             self.handle = None
+            self._c_handle = ctypes.c_void_p(None)
             raise
 
     @classmethod
@@ -322,14 +328,16 @@ class Plan:
         if ptrs != self._last_ptrs:
             self._last_ptrs, self._last_arr = ptrs, _ptr_array(ptrs)
         if stream is None or stream is not self._last_stream:
-            self._last_stream, self._last_handle = stream, _stream_handle(stream)
+            self._last_stream, self._last_handle = stream, ctypes.c_void_p(_stream_handle(stream))
             if stream is None:
                 self._last_stream = _NO_STREAM
         return self._last_arr, self._last_handle
 
     def allreduce(self, rank_bufs, scale, stream=None):
         arr, handle = self._rank_array(rank_bufs, stream)
-        status = _ddl_allreduce(self.handle, arr, scale, handle)
+        if scale != self._scale:
+            self._scale, self._c_scale = scale, ctypes.c_float(scale)
+        status = _ddl_allreduce(self._c_handle, arr, self._c_scale, handle)
         if status:
             raise DDLError(status, "ddl_allreduce")
 
@@ -354,7 +362,7 @@ class Plan:
 
     def allreduce_bucket(self, bucket, rank_bufs, scale, stream=None):
         arr, handle = self._rank_array(rank_bufs, stream)
-        _ok(_lib.ddl_allreduce_bucket(self.handle, bucket, arr, scale, handle), "ddl_allreduce_bucket")
+        _ok(_lib.ddl_allreduce_bucket(self.handle, bucket, arr, scale, handle.value), "ddl_allreduce_bucket")
 
     def allreduce_host(self, host_bufs, dev_bufs, scale, stream=None):
         ddl_allreduce_host(self.handle, host_bufs, dev_bufs, scale, stream)
@@ -411,6 +419,7 @@ class Plan:
         if self.handle is not None:
             ddl_plan_destroy(self.handle)
             self.handle = None
+            self._c_handle = ctypes.c_void_p(None)  # a later call gets DDL_ERR_INVALID_ARG
 
     def __del__(self):
         try:
