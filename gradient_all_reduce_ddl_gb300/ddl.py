@@ -275,6 +275,8 @@ def ddl_noalloc_check(stream=None):
 # given ready-made ctypes arguments (no conversion on each call)
 _ddl_allreduce = ctypes.CDLL(LIB_PATH).ddl_allreduce
 _ddl_allreduce.restype = ctypes.c_int
+_ddl_allreduce_sgd = ctypes.CDLL(LIB_PATH).ddl_allreduce_sgd
+_ddl_allreduce_sgd.restype = ctypes.c_int
 _NO_STREAM = object()  # no stream object seen yet (None means the current stream, looked up each call)
 
 TOPOLOGIES = {"ring": DDL_RING, "multiring": DDL_MULTIRING, "torus": DDL_TORUS, "torus_nd": DDL_RING}
@@ -293,6 +295,7 @@ class Plan:
         self._last_ptrs, self._last_arr = None, None
         self._last_stream, self._last_handle = _NO_STREAM, None
         self._sgd_key, self._sgd_arrs = None, None
+        self._sgd_hyper, self._sgd_c = None, None
         self._scale, self._c_scale = None, None
         topo_t = ddl_topology_t(TOPOLOGIES[topo], int(k), int(X), int(Y))
         self.handle = ddl_plan_create(self.P, self.N, DTYPES[dtype], topo_t, int(bucket_bytes))
@@ -317,21 +320,25 @@ class Plan:
         return cls(w.P, w.N, w.dtype, w.topo, k=w.k, X=w.X, Y=w.Y, bucket_bytes=w.bucket_bytes,
                    layers=w.layers, dims=getattr(w, "dims", None), **kw)
 
+    def _stream_c(self, stream):
+        # the stream handle, kept for the stream object last seen (None: the
+        # current stream, looked up on every call)
+        if stream is None or stream is not self._last_stream:
+            self._last_stream, self._last_handle = stream, ctypes.c_void_p(_stream_handle(stream))
+            if stream is None:
+                self._last_stream = _NO_STREAM
+        return self._last_handle
+
     def _rank_array(self, rank_bufs, stream):
         # the per-call path of small all-reduces: the ctypes pointer array is
-        # rebuilt only when the buffers change, and the stream handle is kept
-        # for the stream object last seen
+        # rebuilt only when the buffers change
         try:
             ptrs = [b.data_ptr() for b in rank_bufs]
         except AttributeError:
             ptrs = _dev_ptrs(rank_bufs)
         if ptrs != self._last_ptrs:
             self._last_ptrs, self._last_arr = ptrs, _ptr_array(ptrs)
-        if stream is None or stream is not self._last_stream:
-            self._last_stream, self._last_handle = stream, ctypes.c_void_p(_stream_handle(stream))
-            if stream is None:
-                self._last_stream = _NO_STREAM
-        return self._last_arr, self._last_handle
+        return self._last_arr, self._stream_c(stream)
 
     def allreduce(self, rank_bufs, scale, stream=None):
         arr, handle = self._rank_array(rank_bufs, stream)
@@ -354,8 +361,13 @@ class Plan:
             self._sgd_key = key
             self._sgd_arrs = (_ptr_array(key[0]), _ptr_array(key[1]), None if key[2] is None else _ptr_array(key[2]))
         g, pa, m = self._sgd_arrs
-        _ok(_lib.ddl_allreduce_sgd(self.handle, g, pa, m, scale, lr, momentum, weight_decay, 1 if keep_grads else 0,
-                                   _stream_handle(stream)), "ddl_allreduce_sgd")
+        hyper = (scale, lr, momentum, weight_decay, bool(keep_grads))
+        if hyper != self._sgd_hyper:  # the scalars as ctypes values, rebuilt when one changes
+            self._sgd_hyper = hyper
+            self._sgd_c = tuple(ctypes.c_float(v) for v in hyper[:4]) + (ctypes.c_int(1 if keep_grads else 0),)
+        status = _ddl_allreduce_sgd(self._c_handle, g, pa, m, *self._sgd_c, self._stream_c(stream))
+        if status:
+            raise DDLError(status, "ddl_allreduce_sgd")
 
     def allreduce_slab(self, base, rank_stride_bytes, scale, stream=None):
         ddl_allreduce_slab(self.handle, base, rank_stride_bytes, scale, stream)
