@@ -739,14 +739,18 @@ ddl_status_t ddl_bucket_ready(ddl_plan_t p, int bucket, void* stream) {
   if (e == cudaSuccess) e = cudaStreamWaitEvent(p->side, p->ev_ready[bucket], 0);
   if (e != cudaSuccess) return cuda_status(e);
   p->ov_issued[bucket] = 1;
-  // With the library's kernel choice the side stream runs the rank-chunked
-  // staged pass: a persistent grid of two CTAs per SM that streams the
-  // bucket's work items, instead of one CTA per item.  Sharing the GPU with
-  // the producer's kernels, it measured faster than the register pass
-  // (ResNet-101 multi-ring, 7 buckets: 9.24 ms overlapped against 9.47 ms
-  // sequential, where the register pass took 10.08 ms).  Same results.
+  // With the library's kernel choice and full-size (8 KB) work items the side
+  // stream runs the rank-chunked staged pass: a persistent grid of two CTAs
+  // per SM that streams the bucket's work items, instead of one CTA per item.
+  // Sharing the GPU with the producer's kernels, it measured faster than the
+  // register pass (ResNet-101 multi-ring, 7 buckets: 9.24 ms overlapped
+  // against 9.47 ms sequential, where the register pass took 10.08 ms).
+  // Smaller items (small buckets) take the library's own pass choice: the
+  // staged pass's persistent grid and pipeline cost several microseconds per
+  // bucket there (4x4 torus, 8 buckets of 32 KB per rank: 54.5 against the
+  // plain all-reduce's 3.7 us).  Same results either way.
   const bool staged = p->kernel == DDL_KERNEL_AUTO && p->spec.topo != ddl::kTorusND &&
-                      p->spec.tile_bytes <= (uint32_t)ddl::kTileBytes;
+                      p->spec.tile_bytes == (uint32_t)ddl::kTileBytes;
   return run_bucket(p, bucket, p->ov_bufs.data(), aligned, p->ov_scale, p->side, false,
                     staged ? ddl::kVarChunked : 0);
 }

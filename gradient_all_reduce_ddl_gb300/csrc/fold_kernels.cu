@@ -1065,8 +1065,11 @@ __host__ __device__ constexpr uint32_t bulk_smem_bytes(uint32_t P, uint32_t tile
          (uint32_t)(kStages * sizeof(BulkMeta)) + (uint32_t)(2 * kStages * sizeof(uint64_t)) + 16u;
 }
 
+// Out of line, as fold_scalar: inlined, its batched loads raised the staged
+// passes' registers (rank-chunked 80 to 94), which share the SMs with the
+// producer's kernels on the overlap side stream.
 template <bool F16>
-__device__ void fold_scalar_ordered(const FoldParams& p, const uint8_t* order, uint64_t e, int inner, int groups,
+__device__ __noinline__ void fold_scalar_ordered(const FoldParams& p, const uint8_t* order, uint64_t e, int inner, int groups,
                                     bool rh) {
   const auto at = [&p, order](int t) { return static_cast<const char*>(p.bufs[order[t]]); };
   const float r = __fmul_rn(fold_elem<F16>(at, e, p.P, inner, groups, rh), p.scale);
