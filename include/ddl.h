@@ -106,7 +106,8 @@ typedef enum {
   DDL_KERNEL_CHUNKED = 5    /* bulk async loads of the register pass's tiles (up to 8 KB per
                                rank) into shared memory, 2 ranks per stage in fold order,
                                the fold kept in registers across an item's stages, stores
-                               from registers (the overlap side stream's kernel) */
+                               from registers (the overlap side stream's kernel for buckets of full-size
+                               8 KB work items; smaller ones take the library's own choice) */
 } ddl_kernel_t;
 
 typedef struct ddl_plan* ddl_plan_t;
