@@ -63,3 +63,36 @@ def test_random_problem_tables_match_oracle(seed):
             assert got[0] == o.tolist(), (kw, i)
             if kw["topo"] != "torus_nd":
                 assert got[1:] == (inner, groups)
+
+
+KERNEL_NAMES = {"fold_ldg_kernel", "fold_small_kernel", "fold_lat_kernel", "fold_lat_kernel (one group)",
+                "fold_nd_kernel", "fold_nd_h2_kernel", "fold_lat_nd_kernel", "fold_bulk_kernel", "fold_chunked_kernel",
+                "step_kernel"}
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_problem_kernel_name(seed):
+    """ddl_plan_kernel_name answers for every drawn shape, mode and kernel
+    choice with one of the library's passes, consistent with the plan's mode
+    and choice (host-only)."""
+    from gradient_all_reduce_ddl_gb300.build import build
+    build()
+    from gradient_all_reduce_ddl_gb300 import ddl
+    rng = np.random.default_rng(3000 + seed)
+    kw = _random_problem(rng)
+    kw["N"] = int(kw["N"]) * int(rng.integers(1, 400))       # up to ~1M elements: every item size
+    if "layers" in kw:
+        kw["layers"] = kw["layers"][:-1] + [kw["layers"][-1] + kw["N"] - sum(kw["layers"])]
+    mode = str(rng.choice(["fused", "stepwise", "rankorder"]))
+    kernel = str(rng.choice(["auto", "ldg", "bulkload", "chunked"]))
+    with ddl.Plan(mode=mode, kernel=kernel, **kw) as plan:
+        name = plan.kernel_name
+    assert name in KERNEL_NAMES, name
+    if mode == "stepwise":
+        assert name == "step_kernel"
+    elif kw["topo"] == "torus_nd" and mode == "fused":
+        assert name in {"fold_nd_kernel", "fold_nd_h2_kernel", "fold_lat_nd_kernel"}
+    elif kernel in ("bulkload", "chunked"):
+        assert name == {"bulkload": "fold_bulk_kernel", "chunked": "fold_chunked_kernel"}[kernel]
+    else:
+        assert name in {"fold_ldg_kernel", "fold_small_kernel", "fold_lat_kernel", "fold_lat_kernel (one group)"}
