@@ -65,9 +65,9 @@ SECONDARY = ("ring4_int", "torus4x4_resnet50", "torus8x4_resnet50_f16", "multiri
 # algorithmic bytes; a changed kernel source reports null.
 NCU_TRAFFIC = {
     # P = 16 x 20,000,000 fp32 (1.28 GB resident, above L2): 2.56 GB algorithmic per launch
-    ("ring", "f32", "ldg", "731287964c7ff06e"): (1_280_196_608 + 1_220_551_424, 2_560_000_000),
-    ("multiring", "f32", "ldg", "731287964c7ff06e"): (1_280_197_376 + 1_220_516_352, 2_560_000_000),
-    ("torus", "f32", "ldg", "731287964c7ff06e"): (1_280_196_352 + 1_220_694_016, 2_560_000_000),
+    ("ring", "f32", "ldg", "878096f0134ae334"): (1_280_214_528 + 1_220_379_392, 2_560_000_000),
+    ("multiring", "f32", "ldg", "878096f0134ae334"): (1_280_397_056 + 1_220_582_400, 2_560_000_000),
+    ("torus", "f32", "ldg", "878096f0134ae334"): (1_280_243_200 + 1_220_768_000, 2_560_000_000),
 }
 
 KERNEL_SOURCES = ["gradient_all_reduce_ddl_gb300/csrc/fold_kernels.cu"]

@@ -1628,7 +1628,8 @@ FoldPass fold_pass(const FoldParams& p, uint32_t n_items, bool f16, int variant)
   const bool unrounded = !f16 || !p.round_hops;
   const bool single = unrounded && p.groups == 1 && p.inner == p.P;
   const bool small_items = p.tile_bytes <= (uint32_t)kThreads * 16u;
-  if (p.vector_ok && small_items && p.P >= kLatMinP && p.groups >= 1 && p.inner >= 1 &&
+  const int lat_min_p = f16 && p.round_hops ? kLatMinPHops : kLatMinP;
+  if (p.vector_ok && small_items && p.P >= lat_min_p && p.groups >= 1 && p.inner >= 1 &&
       (int64_t)p.inner * p.groups == p.P) {
     const uint32_t smem = lat_smem_of(p, f16);
     bool take = smem <= kLatMaxSmem;

@@ -383,6 +383,7 @@ uint32_t ldg_tile_bytes(uint64_t bytes_per_rank, uint32_t floor) {
 
 uint32_t fused_tile_floor(int P, int topo, int Y, int esize, int mode) {
   if (P >= kLatMinP) return 256;
+  if (P >= kLatMinPHops && esize == 2 && mode == kFused && topo != kTorusND) return 256;
   const bool one_group = mode == kRankOrder || topo == kRing || topo == kMultiRing || (topo == kTorus && Y == 1);
   const bool unrounded = mode == kRankOrder || esize == 4;
   return one_group && unrounded ? 256 : 1024;

@@ -87,6 +87,11 @@ uint32_t bulk_tile_bytes(int P);
 #define DDL_LAT_MIN_P 16
 #endif
 constexpr int kLatMinP = DDL_LAT_MIN_P;
+// With binary16 storage and rounded hops the register pass's per-rank chain
+// is longer, and the latency pass already wins from 8 ranks (P = 8 fp16 torus
+// at 16,384 elements: 2.80 against 2.25 us per all-reduce in graph replay;
+// at 262,144: 6.32 against 3.51 us).
+constexpr int kLatMinPHops = 8;
 
 // Work-item size of the register, small-item and latency passes: kTileBytes,
 // or smaller, down to `floor` bytes, when a rank's buffer is too small to give
@@ -94,7 +99,8 @@ constexpr int kLatMinP = DDL_LAT_MIN_P;
 uint32_t ldg_tile_bytes(uint64_t bytes_per_rank, uint32_t floor);
 
 // That floor for a plan: 256 bytes where small buffers take the latency pass
-// (P >= kLatMinP) or the small-item pass (a single fold group with no
+// (P >= kLatMinP, or P >= kLatMinPHops with binary16 hops on a two-level
+// fold) or the small-item pass (a single fold group with no
 // intermediate rounding: rank order, and the binary32 ring, multi-ring and
 // one-row torus), whose time falls with the bytes one CTA stages; 1 KB where
 // they take the register pass, whose fixed costs per CTA then dominate.

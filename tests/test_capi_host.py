@@ -219,7 +219,9 @@ DISPATCH = [
     (dict(P=16, N=25_557_032, topo="torus", X=4, Y=4), "fold_ldg_kernel"),
     (dict(P=32, N=25_557_032, dtype="f16", topo="torus", X=8, Y=4), "fold_ldg_kernel"),
     (dict(P=4, N=65_536), "fold_small_kernel"),
-    (dict(P=8, N=16_384, dtype="f16"), "fold_ldg_kernel"),            # binary16 hops: not unrounded
+    (dict(P=8, N=16_384, dtype="f16"), "fold_lat_kernel (one group)"),  # binary16 hops: the latency pass from P = 8
+    (dict(P=8, N=16_384, dtype="f16", topo="torus", X=4, Y=2), "fold_lat_kernel"),
+    (dict(P=4, N=65_536, dtype="f16"), "fold_ldg_kernel"),            # binary16 hops, P < 8
     (dict(P=8, N=16_384, dtype="f16", mode="rankorder"), "fold_small_kernel"),
     (dict(P=8, N=16_384, topo="torus", X=4, Y=2), "fold_ldg_kernel"),
     (dict(P=16, N=16_384), "fold_lat_kernel (one group)"),
